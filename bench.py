@@ -1,0 +1,387 @@
+"""Throughput benchmark of chunked causal GQA prefill attention on GB300.
+
+One step = one call of the whole hot path (pfa_prefill_attention: QK^T, index
+mask, online softmax, PV, epilogue, all in the library's kernels) over one
+layer's chunk of synthetic, seeded inputs already resident in HBM.  The
+default workload is the Mistral-7B-shaped layer (32 query heads, 8 kv heads,
+head_dim 128, a 1358-token prompt, bf16); --workload selects another.
+
+Timing: W untimed warm-up steps; then K steps, each preceded (outside its
+timed span) by a 256 MiB write that flushes L2, each timed with CUDA events on
+the launching stream; barrier + synchronize on both sides; max over ranks.
+Metric: causal attention TFLOP/s = 4 * head_dim * num_heads * (sum over query
+tokens of visible keys) / time, 2 flops per multiply-add.
+
+--impl reference times the fp64 CPU oracle (the reference arm) on the host's
+cores on a bounded sample of the same workload.
+
+Under torchrun every rank runs its own replica of the workload on its own GPU
+(no data exchange: the path shards by kv head and the replicas are
+independent), and rank 0 prints one JSON line.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "prefill-attention TFLOP/s (causal) & prompt-tok/s per layer; % of bf16 peak"
+KERNEL_SOURCES = {
+    "bf16_d128": "chunked_causal_gqa_gb300/csrc/pfa_bf16_d128.cu",
+    "f32": "chunked_causal_gqa_gb300/csrc/pfa_f32.cu",
+}
+
+
+def dist_env():
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return rank, world, local
+
+
+def kernel_name(wl) -> str:
+    return "f32" if wl.dtype == "f32" else f"bf16_d{wl.head_dim}"
+
+
+def source_hash(name: str) -> str:
+    path = os.path.join(ROOT, KERNEL_SOURCES.get(name, ""))
+    if not os.path.isfile(path):
+        return ""
+    h = hashlib.sha256()
+    for p in (path, os.path.join(ROOT, "chunked_causal_gqa_gb300/csrc/pfa_ptx.cuh")):
+        with open(p, "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def measured_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            return json.load(f), "measured"
+    except (OSError, ValueError):
+        return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}, \
+            "fallback"
+
+
+def recorded_traffic(kernel: str, workload: str):
+    """dram read+write bytes per launch from a committed ncu summary, or None
+    if none exists for this kernel/workload or the kernel changed since."""
+    path = os.path.join(ROOT, "profiles", "traffic.txt")
+    if not os.path.isfile(path):
+        return None
+    want = source_hash(kernel)
+    with open(path) as f:
+        for line in f:
+            parts = line.split()
+            if len(parts) >= 4 and not line.startswith("#") and parts[0] == kernel \
+                    and parts[1] == workload and parts[2] == want:
+                return float(parts[3])
+    return None
+
+
+class ClockSampler:
+    """Samples SM clocks and throttle reasons with nvidia-smi while running."""
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines = []
+        self.thread = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except (OSError, ValueError):
+            self.proc = None
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+        time.sleep(0.3)
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        if self.thread:
+            self.thread.join(timeout=2)
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in self.lines:
+            f = [x.strip() for x in line.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                smax.append(float(f[2]))
+            except ValueError:
+                continue
+            for n, val in zip(names, f[5:9]):
+                if val.lower().startswith("active"):
+                    reasons.add(n)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(smax),
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def oracle_sample(wl, budget_s: float):
+    """Time the fp64 oracle on the host cores over a bounded sample of the
+    workload's (token, head) rows.  Returns (flops/s, description, cores)."""
+    import numpy as np
+
+    import oracle
+    from chunked_causal_gqa_gb300 import workloads as W
+
+    q, k, v = W.make_inputs(wl)
+    cores = oracle.default_threads()
+    # estimate per-row cost from the visible key count; take evenly spaced rows
+    T, H = wl.T, wl.num_heads
+    total_rows = T * H
+    flops_total = wl.causal_flops()
+    # calibration: a small sample
+    rows_all = [(t, h) for t in range(T) for h in range(H)]
+    step = max(1, total_rows // 256)
+    calib = rows_all[::step]
+    t0 = time.perf_counter()
+    oracle.prefill_attention_rows(q, k, v, calib, window=wl.window, scale=wl.scale,
+                                  threads=cores)
+    dt = max(time.perf_counter() - t0, 1e-3)
+    calib_flops = sum(4.0 * wl.head_dim * _visible(wl, t) for t, _ in calib)
+    rate = calib_flops / dt
+    n_rows = int(min(total_rows, max(len(calib), budget_s * rate /
+                                     max(flops_total / total_rows, 1.0))))
+    if n_rows >= total_rows:
+        t0 = time.perf_counter()
+        oracle.prefill_attention(q, k, v, window=wl.window, scale=wl.scale, threads=cores)
+        dt = time.perf_counter() - t0
+        return flops_total / dt, f"full workload ({total_rows} rows)", cores, dt
+    step = max(1, total_rows // n_rows)
+    rows = rows_all[::step]
+    sample_flops = sum(4.0 * wl.head_dim * _visible(wl, t) for t, _ in rows)
+    t0 = time.perf_counter()
+    oracle.prefill_attention_rows(q, k, v, rows, window=wl.window, scale=wl.scale, threads=cores)
+    dt = time.perf_counter() - t0
+    return sample_flops / dt, f"{len(rows)} of {total_rows} (token, head) rows, every {step}th", \
+        cores, dt
+
+
+def _visible(wl, t):
+    pos = wl.start_pos + t
+    return min(pos + 1, wl.window) if wl.window > 0 else pos + 1
+
+
+def run_reference(args, wl):
+    rank, world, _ = dist_env()
+    if rank != 0:
+        return 0
+    times, descr, cores = [], "", 1
+    budget = max(1.0, args.ref_seconds / max(1, args.steps + args.warmup))
+    flops_s = []
+    for i in range(args.warmup + args.steps):
+        rate, descr, cores, dt = oracle_sample(wl, budget)
+        if i >= args.warmup:
+            flops_s.append(rate)
+            times.append(dt)
+    value = statistics.mean(flops_s) / 1e12
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s",
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": 1e3 * statistics.mean(times), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": wl.name, "description": wl.description},
+        "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
+                         "sample": descr},
+        "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def run_ours(args, wl):
+    import torch
+    import torch.distributed as dist
+
+    import chunked_causal_gqa_gb300 as pkg
+    from chunked_causal_gqa_gb300 import workloads as W
+
+    rank, world, local = dist_env()
+    if world > 1:
+        dist.init_process_group("nccl" if torch.cuda.is_available() else "gloo")
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+
+    q_h, k_h, v_h = W.make_inputs(wl)
+    q, k, v = q_h.to(dev), k_h.to(dev), v_h.to(dev)
+    out = torch.empty_like(q)
+    flush = torch.empty(256 * 1024 * 1024, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def step():
+        pkg.prefill_attention(q, k, v, out=out, window=wl.window, scale=wl.scale)
+
+    for _ in range(args.warmup):
+        flush.fill_(1)
+        step()
+    torch.cuda.synchronize(dev)
+    if pkg.last_device_error() != 0:
+        raise RuntimeError("device error during warm-up")
+
+    sampler = ClockSampler(int(os.environ.get("CUDA_VISIBLE_DEVICES", str(local)).split(",")[0])
+                           if os.environ.get("CUDA_VISIBLE_DEVICES", "").isdigit() else local)
+    sampler.start()
+    # one sustained burst so that the clock sampler sees the GPU under load
+    events = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+              for _ in range(args.steps)]
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize(dev)
+    wall0 = time.perf_counter()
+    for e0, e1 in events:
+        flush.fill_(1)
+        e0.record(stream)
+        step()
+        e1.record(stream)
+    torch.cuda.synchronize(dev)
+    wall = time.perf_counter() - wall0
+    if world > 1:
+        dist.barrier()
+    clocks = sampler.stop()
+    status = pkg.last_device_error()
+    if status != 0:
+        raise RuntimeError(f"device error status {status} in the timed region")
+    per = [e0.elapsed_time(e1) for e0, e1 in events]
+    ms = statistics.mean(per)
+    total_ms = sum(per)
+    if world > 1:
+        t = torch.tensor([total_ms], dtype=torch.float64, device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        total_ms = float(t.item())
+    ms_step = total_ms / args.steps
+    flops = wl.causal_flops()
+    value = world * flops / (ms_step * 1e-3) / 1e12
+
+    # ---- end to end through the public API with host buffers
+    e2e = None
+    if not args.no_e2e:
+        qp, kp, vp = q_h.pin_memory(), k_h.pin_memory(), v_h.pin_memory()
+        outp = torch.empty_like(qp).pin_memory()
+        h2d = sum(x.numel() * x.element_size() for x in (qp, kp, vp))
+        d2h = outp.numel() * outp.element_size()
+        n_e2e = max(3, min(args.steps, 50))
+        for _ in range(2):
+            pkg.prefill_attention(qp, kp, vp, out=outp, window=wl.window, scale=wl.scale)
+        torch.cuda.synchronize(dev)
+        t0 = time.perf_counter()
+        for _ in range(n_e2e):
+            pkg.prefill_attention(qp, kp, vp, out=outp, window=wl.window, scale=wl.scale)
+        torch.cuda.synchronize(dev)
+        e2e_s = (time.perf_counter() - t0) / n_e2e
+        if world > 1:
+            t = torch.tensor([e2e_s], dtype=torch.float64, device=dev)
+            dist.all_reduce(t, op=dist.ReduceOp.MAX)
+            e2e_s = float(t.item())
+        e2e = {"value": world * flops / e2e_s / 1e12, "unit": "TFLOP/s",
+               "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+               "ms_per_step": 1e3 * e2e_s}
+
+    peaks, peak_src = measured_peaks()
+    kname = kernel_name(wl)
+    if wl.dtype == "f32":
+        # fp32 SIMT path: bound by the fp32 FMA pipe
+        peak = 2.0 * 128 * 152 * (peaks.get("sm_max_mhz", 2070.0) * 1e6) / 1e12
+        bound, peak_note = "alu", "fp32 FMA: 128 lanes x 2 flops x 152 SMs x max SM clock"
+    else:
+        peak = float(peaks["bf16_tflops"])
+        bound, peak_note = "tensor", f"bf16_tflops ({peak_src}, burst)"
+    achieved = flops / (ms * 1e-3) / 1e12
+    roofline = {"bound": bound, "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
+                "frac": achieved / peak, "traffic": recorded_traffic(kname, wl.name),
+                "kernel": kname, "peak_source": peak_note,
+                "algorithmic_bytes": wl.algorithmic_bytes()}
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        rate, descr, cores, _ = oracle_sample(wl, args.cpu_seconds)
+        cpu = {"value": rate / 1e12, "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
+               "sample": descr}
+
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_step,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": wl.dtype, "data": "synthetic",
+            "config": {"workload": wl.name, "description": wl.description,
+                       "num_heads": wl.num_heads, "num_kv_heads": wl.num_kv_heads,
+                       "head_dim": wl.head_dim, "T": wl.T, "start_pos": wl.start_pos,
+                       "window": wl.window, "seeds": list(wl.seeds),
+                       "l2": "flushed before every timed step (256 MiB write)",
+                       "parallelism": f"replicas x{world}"},
+            "prompt_tok_s_per_layer": world * wl.T / (ms_step * 1e-3),
+            "frac_of_bf16_peak": value / world / float(peaks["bf16_tflops"]),
+            "ms_min": min(per), "ms_median": statistics.median(per),
+            "wall_s_timed": wall,
+            "gpu_launches": args.steps * launches_per_step(wl),
+            "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e, "clocks": clocks,
+        }
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+    return 0
+
+
+def launches_per_step(wl) -> int:
+    return 1
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default="mistral_1358")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=15.0,
+                    help="CPU-baseline sample budget (oracle seconds)")
+    ap.add_argument("--ref-seconds", type=float, default=60.0,
+                    help="reference-arm budget over all its steps (oracle seconds)")
+    args = ap.parse_args(argv)
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    from chunked_causal_gqa_gb300 import workloads as W
+    wl = W.WORKLOADS[args.workload]
+    if args.impl == "reference":
+        return run_reference(args, wl)
+    return run_ours(args, wl)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

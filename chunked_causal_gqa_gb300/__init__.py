@@ -1,0 +1,123 @@
+"""GB300-native chunked causal GQA prefill attention.
+
+A chunk of T query tokens at absolute positions start_pos .. start_pos+T-1
+attends to the L = start_pos + T keys of a KV cache: query head h reads kv
+head h / (num_heads / num_kv_heads), scores are scaled, key j is masked unless
+j <= start_pos + t (and, with a sliding window, j > start_pos + t - window),
+and a row softmax weights the sum of V (gnosis "Prefill attention -> GPU:
+handoff", section "GPU design").
+
+The computation runs in libpfa.so, a C-ABI library of hand-written sm_103a
+kernels (include/pfa.h).  This package is its thin Python binding: it checks
+tensors, passes pointers and the current CUDA stream, and copies host tensors
+to and from the device when it is handed CPU tensors.
+"""
+from __future__ import annotations
+
+import math
+
+import torch
+
+from . import _binding
+from ._binding import PFA_BF16, PFA_F32, PfaError
+
+__all__ = ["prefill_attention", "last_device_error", "status_string", "version",
+           "debug_configure", "PfaError", "PFA_F32", "PFA_BF16"]
+
+_DTYPES = {torch.float32: PFA_F32, torch.bfloat16: PFA_BF16}
+
+
+def _stream_handle(device: torch.device, stream) -> int:
+    if stream is None:
+        stream = torch.cuda.current_stream(device)
+    return int(stream.cuda_stream)
+
+
+def prefill_attention(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor,
+                      out: torch.Tensor | None = None, *, start_pos: int | None = None,
+                      window: int = 0, scale: float | None = None, stream=None) -> torch.Tensor:
+    """Chunked causal GQA prefill attention through pfa_prefill_attention.
+
+    q: [T, num_heads, head_dim]; k_cache, v_cache: [num_kv_heads, L, head_dim]
+    with L = start_pos + T (start_pos defaults to L - T); all contiguous, of
+    one dtype (float32 or bfloat16).  window <= 0 means global causal.  scale
+    defaults to 1/sqrt(head_dim) rounded to float32.
+
+    CUDA tensors: the call is enqueued on `stream` (default: the current
+    stream) and returns without synchronising.  CPU tensors: they are copied to
+    the current CUDA device, the kernel runs, and the result is copied back
+    (the copy back synchronises).
+    """
+    if q.dim() != 3 or k_cache.dim() != 3 or v_cache.dim() != 3:
+        raise ValueError("q must be [T, H, D]; k_cache and v_cache [Hkv, L, D]")
+    if k_cache.shape != v_cache.shape:
+        raise ValueError("k_cache and v_cache shapes differ")
+    if q.dtype not in _DTYPES or k_cache.dtype != q.dtype or v_cache.dtype != q.dtype:
+        raise ValueError("q, k_cache and v_cache must all be float32 or all bfloat16")
+    T, H, D = q.shape
+    Hkv, L, Dk = k_cache.shape
+    if Dk != D:
+        raise ValueError("head_dim of q and the cache differ")
+    if start_pos is None:
+        start_pos = L - T
+    if start_pos < 0 or start_pos + T != L:
+        raise ValueError(f"cache length {L} must equal start_pos + T = {start_pos + T}")
+    if scale is None:
+        scale = float(torch.tensor(1.0 / math.sqrt(D), dtype=torch.float32))
+
+    host = q.device.type == "cpu"
+    if host:
+        dev = torch.device("cuda", torch.cuda.current_device())
+        qd = q.to(dev, non_blocking=True)
+        kd = k_cache.to(dev, non_blocking=True)
+        vd = v_cache.to(dev, non_blocking=True)
+        od = torch.empty_like(qd)
+    else:
+        if k_cache.device != q.device or v_cache.device != q.device:
+            raise ValueError("q, k_cache and v_cache must be on one device")
+        dev = q.device
+        qd, kd, vd = q, k_cache, v_cache
+        od = out if out is not None else torch.empty_like(q)
+        if od.shape != q.shape or od.dtype != q.dtype or od.device != q.device:
+            raise ValueError("out must match q in shape, dtype and device")
+    for name, t in (("q", qd), ("k_cache", kd), ("v_cache", vd), ("out", od)):
+        if not t.is_contiguous():
+            raise ValueError(f"{name} must be contiguous")
+
+    lib = _binding.load()
+    with torch.cuda.device(dev):
+        st = _stream_handle(dev, stream)
+        rc = lib.pfa_prefill_attention(qd.data_ptr(), kd.data_ptr(), vd.data_ptr(), od.data_ptr(),
+                                       int(T), int(start_pos), int(H), int(Hkv), int(D),
+                                       int(window), float(scale), _DTYPES[q.dtype], st)
+    if rc != 0:
+        raise PfaError(rc, "pfa_prefill_attention")
+    if host:
+        res = od.to("cpu")
+        if out is not None:
+            out.copy_(res)
+            return out
+        return res
+    return od
+
+
+def last_device_error(stream=None, device=None) -> int:
+    """Synchronise the stream and return (and clear) the device error status."""
+    dev = torch.device("cuda", torch.cuda.current_device()) if device is None else device
+    lib = _binding.load()
+    with torch.cuda.device(dev):
+        return lib.pfa_last_device_error(_stream_handle(dev, stream))
+
+
+def status_string(status: int) -> str:
+    return _binding.load().pfa_status_string(int(status)).decode()
+
+
+def version() -> tuple:
+    v = _binding.load().pfa_version()
+    return (v >> 16, v & 0xFFFF)
+
+
+def debug_configure(wait_limit_ms: float = 0.0, force_timeout: bool = False) -> None:
+    """Device-side wait limit and the forced-timeout test hook (see pfa.h)."""
+    _binding.load().pfa_debug_configure(float(wait_limit_ms), 1 if force_timeout else 0)

@@ -1,0 +1,304 @@
+// pfa_api.cu -- the C ABI of libpfa (declared in include/pfa.h): argument
+// validation, per-device state, the device error word, cached TMA tensor-map
+// descriptors and kernel dispatch.
+//
+// The entry point follows the gate discipline of the gnosis page "Prefill
+// attention -> GPU: handoff" (section "GPU design", correctness gate: any
+// unsupported shape or GPU error is reported to the caller, who may fall back)
+// as status codes: nothing here aborts, traps or prints unless PFA_TRACE is set.
+#include "pfa_internal.h"
+#include "pfa_ptx.cuh"
+
+#include "../../include/pfa.h"
+
+#include <cmath>
+#include <cstdio>
+#include <cstdlib>
+#include <cstring>
+#include <mutex>
+#include <unordered_map>
+
+namespace pfa {
+namespace {
+
+// Device-side error word (one per device context).  Kernels receive its
+// address and atomically OR error bits into it.
+__device__ unsigned int g_error_word;
+
+struct DeviceState {
+  bool ready = false;
+  int status = kOk;       // kOk, or kErrDevice if the device is unusable
+  int num_sms = 0;
+  unsigned* err = nullptr;
+};
+
+std::mutex g_mutex;
+DeviceState g_dev[64];
+double g_wait_limit_ms = 2000.0;
+int g_force_timeout = 0;
+
+bool trace_on() {
+  static const int on = [] {
+    const char* e = std::getenv("PFA_TRACE");
+    return (e && *e && std::strcmp(e, "0") != 0) ? 1 : 0;
+  }();
+  return on != 0;
+}
+
+// Per-device set-up: compute capability check, SM count, error word address.
+int device_state(int* dev_out, DeviceState** st_out) {
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) {
+    cudaGetLastError();
+    return kErrDevice;
+  }
+  std::lock_guard<std::mutex> lk(g_mutex);
+  DeviceState& s = g_dev[dev];
+  if (!s.ready) {
+    int major = 0, minor = 0, sms = 0;
+    if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) {
+      cudaGetLastError();
+      return kErrDevice;
+    }
+    // The library is compiled for sm_103a only.
+    s.status = (major == 10 && minor == 3) ? kOk : kErrDevice;
+    s.num_sms = sms;
+    if (s.status == kOk) {
+      void* addr = nullptr;
+      if (cudaGetSymbolAddress(&addr, g_error_word) != cudaSuccess) {
+        cudaGetLastError();
+        return kErrDevice;
+      }
+      s.err = static_cast<unsigned*>(addr);
+      if (cudaMemset(s.err, 0, sizeof(unsigned)) != cudaSuccess) {
+        cudaGetLastError();
+        return kErrDevice;
+      }
+    }
+    s.ready = true;
+  }
+  *dev_out = dev;
+  *st_out = &s;
+  return s.status;
+}
+
+// A pointer the GPU can read: device memory or managed memory of this device.
+bool device_accessible(const void* p, int dev) {
+  cudaPointerAttributes a;
+  if (cudaPointerGetAttributes(&a, p) != cudaSuccess) {
+    cudaGetLastError();
+    return false;
+  }
+  if (a.type == cudaMemoryTypeManaged) return true;
+  return a.type == cudaMemoryTypeDevice && a.device == dev;
+}
+
+bool overlaps(const void* a, size_t na, const void* b, size_t nb) {
+  const uintptr_t x = reinterpret_cast<uintptr_t>(a), y = reinterpret_cast<uintptr_t>(b);
+  return x < y + nb && y < x + na;
+}
+
+// ------------------------------------------------------------------ TMA maps
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                   const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                   const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = [] {
+    void* f = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault,
+                                         &q) != cudaSuccess ||
+        q != cudaDriverEntryPointSuccess) {
+      cudaGetLastError();
+      return (EncodeTiledFn) nullptr;
+    }
+    return reinterpret_cast<EncodeTiledFn>(f);
+  }();
+  return fn;
+}
+
+struct MapKey {
+  const void* base;
+  uint64_t d0, d1, d2, s0, s1;
+  uint32_t b0, b1, b2;
+  bool operator==(const MapKey& o) const {
+    return base == o.base && d0 == o.d0 && d1 == o.d1 && d2 == o.d2 && s0 == o.s0 &&
+           s1 == o.s1 && b0 == o.b0 && b1 == o.b1 && b2 == o.b2;
+  }
+};
+struct MapKeyHash {
+  size_t operator()(const MapKey& k) const {
+    uint64_t h = reinterpret_cast<uintptr_t>(k.base);
+    const uint64_t v[8] = {k.d0, k.d1, k.d2, k.s0, k.s1, k.b0, k.b1, k.b2};
+    for (uint64_t x : v) h = (h ^ x) * 0x100000001b3ull;
+    return (size_t)h;
+  }
+};
+std::mutex g_map_mutex;
+std::unordered_map<MapKey, CUtensorMap, MapKeyHash> g_maps;
+
+}  // namespace
+
+int encode_tmap_bf16_3d(CUtensorMap* out, const void* base, const uint64_t dims[3],
+                        const uint64_t strides_bytes[2], const uint32_t box[3]) {
+  const MapKey key{base, dims[0], dims[1], dims[2], strides_bytes[0], strides_bytes[1],
+                   box[0], box[1], box[2]};
+  {
+    std::lock_guard<std::mutex> lk(g_map_mutex);
+    auto it = g_maps.find(key);
+    if (it != g_maps.end()) {
+      *out = it->second;
+      return 0;
+    }
+  }
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) return -1;
+  const cuuint64_t gdim[3] = {dims[0], dims[1], dims[2]};
+  const cuuint64_t gstride[2] = {strides_bytes[0], strides_bytes[1]};
+  const cuuint32_t bdim[3] = {box[0], box[1], box[2]};
+  const cuuint32_t estride[3] = {1, 1, 1};
+  CUtensorMap m;
+  std::memset(&m, 0, sizeof(m));
+  const CUresult r = fn(&m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), gdim,
+                        gstride, bdim, estride, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                        CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return -1;
+  {
+    std::lock_guard<std::mutex> lk(g_map_mutex);
+    if (g_maps.size() > 1024) g_maps.clear();
+    g_maps.emplace(key, m);
+  }
+  *out = m;
+  return 0;
+}
+
+}  // namespace pfa
+
+using namespace pfa;
+
+extern "C" {
+
+int pfa_version(void) { return (1 << 16) | 0; }
+
+const char* pfa_status_string(int status) {
+  switch (status) {
+    case PFA_OK: return "PFA_OK";
+    case PFA_ERR_NULL: return "PFA_ERR_NULL: a required pointer is NULL";
+    case PFA_ERR_SHAPE: return "PFA_ERR_SHAPE: unsupported or invalid shape";
+    case PFA_ERR_DTYPE: return "PFA_ERR_DTYPE: unknown dtype";
+    case PFA_ERR_ALIGNMENT: return "PFA_ERR_ALIGNMENT: pointer not 16-byte aligned";
+    case PFA_ERR_DEVICE: return "PFA_ERR_DEVICE: no usable sm_103 device or pointer not on it";
+    case PFA_ERR_LAUNCH: return "PFA_ERR_LAUNCH: the CUDA runtime refused the launch";
+    case PFA_ERR_TIMEOUT: return "PFA_ERR_TIMEOUT: a device-side wait gave up";
+    case PFA_ERR_VALUE: return "PFA_ERR_VALUE: scale is not finite";
+    case PFA_ERR_ALIAS: return "PFA_ERR_ALIAS: out overlaps an input";
+    default: return "PFA: unknown status";
+  }
+}
+
+int pfa_debug_configure(double wait_limit_ms, int force_timeout) {
+  std::lock_guard<std::mutex> lk(g_mutex);
+  g_wait_limit_ms = (wait_limit_ms > 0.0) ? wait_limit_ms : 2000.0;
+  g_force_timeout = force_timeout ? 1 : 0;
+  return PFA_OK;
+}
+
+int pfa_prefill_attention(const void* q, const void* k_cache, const void* v_cache, void* out,
+                          int64_t T, int64_t start_pos, int num_heads, int num_kv_heads,
+                          int head_dim, int window, float scale, int dtype, void* stream) {
+  // ---- pure argument checks (no CUDA calls)
+  if (dtype != PFA_F32 && dtype != PFA_BF16) return PFA_ERR_DTYPE;
+  if (T < 0 || start_pos < 0 || num_heads <= 0 || num_kv_heads <= 0) return PFA_ERR_SHAPE;
+  if (num_heads % num_kv_heads != 0) return PFA_ERR_SHAPE;
+  const int group = num_heads / num_kv_heads;
+  if (dtype == PFA_BF16) {
+    if (head_dim != 128) return PFA_ERR_SHAPE;
+    if (group > 128) return PFA_ERR_SHAPE;
+  } else {
+    if (head_dim <= 0 || head_dim > 512 || head_dim % 4 != 0) return PFA_ERR_SHAPE;
+  }
+  const int64_t L = start_pos + T;
+  // TMA coordinates and launch indices are 32-bit.
+  if (L > ((int64_t)1 << 31) - 4096 || T > ((int64_t)1 << 31) - 4096) return PFA_ERR_SHAPE;
+  if (!std::isfinite(scale)) return PFA_ERR_VALUE;
+  if (T == 0) return PFA_OK;
+  if (!q || !k_cache || !v_cache || !out) return PFA_ERR_NULL;
+  const uintptr_t mis = reinterpret_cast<uintptr_t>(q) | reinterpret_cast<uintptr_t>(k_cache) |
+                        reinterpret_cast<uintptr_t>(v_cache) | reinterpret_cast<uintptr_t>(out);
+  if (mis & 15u) return PFA_ERR_ALIGNMENT;
+  const size_t es = dtype == PFA_F32 ? 4 : 2;
+  const size_t qo_bytes = (size_t)T * num_heads * head_dim * es;
+  const size_t kv_bytes = (size_t)num_kv_heads * (size_t)L * head_dim * es;
+  if (overlaps(out, qo_bytes, q, qo_bytes) || overlaps(out, qo_bytes, k_cache, kv_bytes) ||
+      overlaps(out, qo_bytes, v_cache, kv_bytes))
+    return PFA_ERR_ALIAS;
+
+  // ---- device checks
+  int dev = -1;
+  DeviceState* st = nullptr;
+  const int ds = device_state(&dev, &st);
+  if (ds != kOk) return ds;
+  if (!device_accessible(q, dev) || !device_accessible(k_cache, dev) ||
+      !device_accessible(v_cache, dev) || !device_accessible(out, dev))
+    return PFA_ERR_DEVICE;
+
+  Call c;
+  c.q = q;
+  c.k = k_cache;
+  c.v = v_cache;
+  c.out = out;
+  c.T = T;
+  c.start_pos = start_pos;
+  c.H = num_heads;
+  c.Hkv = num_kv_heads;
+  c.D = head_dim;
+  c.window = window > 0 ? window : 0;
+  c.scale = scale;
+  c.stream = static_cast<cudaStream_t>(stream);
+  c.err = st->err;
+  {
+    std::lock_guard<std::mutex> lk(g_mutex);
+    c.wait_limit_ns = (uint64_t)(g_wait_limit_ms * 1e6);
+    c.flags = g_force_timeout ? kFlagForceTimeout : 0;
+  }
+  c.device = dev;
+  c.num_sms = st->num_sms;
+
+  int rc;
+  if (dtype == PFA_F32)
+    rc = launch_f32(c);
+  else
+    rc = launch_bf16_d128(c);
+  if (trace_on())
+    std::fprintf(stderr, "[pfa] dtype=%d T=%lld start_pos=%lld H=%d Hkv=%d D=%d window=%d -> %d\n",
+                 dtype, (long long)T, (long long)start_pos, num_heads, num_kv_heads, head_dim,
+                 c.window, rc);
+  return rc;
+}
+
+int pfa_last_device_error(void* stream) {
+  int dev = -1;
+  DeviceState* st = nullptr;
+  const int ds = device_state(&dev, &st);
+  if (ds != kOk) return ds;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (cudaStreamSynchronize(s) != cudaSuccess) {
+    cudaGetLastError();
+    return PFA_ERR_DEVICE;
+  }
+  unsigned word = 0;
+  if (cudaMemcpyAsync(&word, st->err, sizeof(word), cudaMemcpyDeviceToHost, s) != cudaSuccess ||
+      cudaMemsetAsync(st->err, 0, sizeof(unsigned), s) != cudaSuccess ||
+      cudaStreamSynchronize(s) != cudaSuccess) {
+    cudaGetLastError();
+    return PFA_ERR_DEVICE;
+  }
+  return (word & kErrTimeout) ? PFA_ERR_TIMEOUT : PFA_OK;
+}
+
+}  // extern "C"

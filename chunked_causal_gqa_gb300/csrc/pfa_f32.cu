@@ -1,0 +1,181 @@
+// pfa_f32.cu -- fp32 prefill attention on the CUDA cores (exact fp32 FMA).
+//
+// Serves the fp32 dtype, whose accuracy bar is max |gpu - fp64| <= 1e-4 (the
+// bar of the gnosis page "Prefill attention -> GPU: handoff", section
+// "Implementation status", GPU-vs-CPU parity).  The tensor cores' tf32 mode
+// keeps only 10 mantissa bits, so this path stays on fp32 FMAs.
+//
+// Work decomposition: a block owns one kv head and 8 consecutive rows of that
+// head's token-major row set (row r -> token r / group, query head
+// kv_head * group + r % group), one warp per row, so every K/V tile staged in
+// shared memory is read by all query heads of the GQA group.  Keys stream in
+// tiles of 32: lane j scores key j of the tile (a full dot product against the
+// warp's query row), the warp takes the tile maximum and sum with shuffles,
+// updates its online-softmax state and accumulates P.V with each lane owning
+// head_dim / 32 output columns.  The causal / window mask is evaluated from
+// the indices; no mask tensor exists.
+#include "pfa_internal.h"
+#include "pfa_ptx.cuh"
+
+#include <cmath>
+
+namespace pfa {
+namespace {
+
+constexpr int kRowsPerBlock = 8;      // one warp per row
+constexpr int kKeysPerTile = 32;
+constexpr int kMaxD = 512;
+constexpr int kMaxCols = kMaxD / 32;  // output columns per lane
+
+struct F32Params {
+  const float* q;
+  const float* k;
+  const float* v;
+  float* out;
+  int64_t T, start_pos, L;
+  int H, Hkv, group, D, window;
+  float scale_log2;        // scale * log2(e)
+  int64_t rows_per_head;   // T * group
+};
+
+__device__ __forceinline__ float warp_max(float x) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) x = fmaxf(x, __shfl_xor_sync(0xffffffffu, x, o));
+  return x;
+}
+__device__ __forceinline__ float warp_sum(float x) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) x += __shfl_xor_sync(0xffffffffu, x, o);
+  return x;
+}
+
+__global__ void __launch_bounds__(kRowsPerBlock * 32)
+f32_attention_kernel(const F32Params p) {
+  extern __shared__ float smem[];
+  const int D = p.D;
+  const int Dp = D + 1;                        // padded K rows: conflict-free column reads
+  float* sK = smem;                            // [32][D+1]
+  float* sV = sK + kKeysPerTile * Dp;          // [32][D]
+  float* sQ = sV + kKeysPerTile * D;           // [8][D]
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int kh = blockIdx.y;
+  const int64_t r0 = (int64_t)blockIdx.x * kRowsPerBlock;
+  const int64_t r = r0 + warp;
+  const bool active = r < p.rows_per_head;
+  const int64_t t = active ? r / p.group : 0;
+  const int h = kh * p.group + (active ? (int)(r % p.group) : 0);
+  const int64_t pos = p.start_pos + t;
+
+  for (int d = lane; d < D; d += 32)
+    sQ[warp * D + d] = active ? p.q[(t * p.H + h) * (int64_t)D + d] : 0.f;
+
+  // Keys any row of this block can see.
+  const int64_t r_last = min(r0 + kRowsPerBlock, p.rows_per_head) - 1;
+  const int64_t pos_lo = p.start_pos + r0 / p.group;
+  const int64_t pos_hi = p.start_pos + r_last / p.group;
+  const int64_t kmin = p.window > 0 ? max((int64_t)0, pos_lo - p.window + 1) : 0;
+  const int64_t kmax = pos_hi;
+
+  const float* kbase = p.k + (int64_t)kh * p.L * D;
+  const float* vbase = p.v + (int64_t)kh * p.L * D;
+  const int ncols = (D + 31) >> 5;
+
+  float m = -INFINITY, l = 0.f;
+  float o[kMaxCols];
+#pragma unroll
+  for (int c = 0; c < kMaxCols; ++c) o[c] = 0.f;
+
+  for (int64_t j0 = kmin; j0 <= kmax; j0 += kKeysPerTile) {
+    __syncthreads();  // previous tile fully consumed (and sQ written, first pass)
+    for (int idx = threadIdx.x; idx < kKeysPerTile * D; idx += blockDim.x) {
+      const int jj = idx / D, d = idx - jj * D;
+      const int64_t j = j0 + jj;
+      float kx = 0.f, vx = 0.f;
+      if (j <= kmax) {
+        kx = kbase[j * D + d];
+        vx = vbase[j * D + d];
+      }
+      sK[jj * Dp + d] = kx;
+      sV[jj * D + d] = vx;
+    }
+    __syncthreads();
+
+    // lane scores key j0 + lane
+    const int64_t j = j0 + lane;
+    const float* qr = sQ + warp * D;
+    const float* kr = sK + lane * Dp;
+    float s = 0.f;
+    for (int d = 0; d < D; ++d) s = fmaf(qr[d], kr[d], s);
+    const bool vis = active && j <= pos && (p.window <= 0 || j > pos - p.window);
+    const float x = vis ? s * p.scale_log2 : -INFINITY;
+
+    const float m_new = fmaxf(m, warp_max(x));
+    const float base = (m_new == -INFINITY) ? 0.f : m_new;   // no visible key yet
+    const float alpha = ex2(m - base);                        // 0 when m = -inf
+    const float pj = ex2(x - base);
+    l = l * alpha + warp_sum(pj);
+#pragma unroll
+    for (int c = 0; c < kMaxCols; ++c) o[c] *= alpha;
+    for (int jj = 0; jj < kKeysPerTile; ++jj) {
+      const float pb = __shfl_sync(0xffffffffu, pj, jj);
+      const float* vr = sV + jj * D;
+#pragma unroll
+      for (int c = 0; c < kMaxCols; ++c) {
+        const int d = lane + 32 * c;
+        if (c < ncols && d < D) o[c] = fmaf(pb, vr[d], o[c]);
+      }
+    }
+    m = m_new;
+  }
+
+  if (active) {
+    const float inv = 1.f / l;
+    float* orow = p.out + (t * p.H + h) * (int64_t)D;
+#pragma unroll
+    for (int c = 0; c < kMaxCols; ++c) {
+      const int d = lane + 32 * c;
+      if (c < ncols && d < D) orow[d] = o[c] * inv;
+    }
+  }
+}
+
+size_t smem_bytes(int D) {
+  return sizeof(float) * ((size_t)kKeysPerTile * (D + 1) + (size_t)kKeysPerTile * D +
+                          (size_t)kRowsPerBlock * D);
+}
+
+}  // namespace
+
+int launch_f32(const Call& c) {
+  static int attr_done[64] = {0};
+  const size_t smem = smem_bytes(c.D);
+  if (c.device >= 0 && c.device < 64 && !attr_done[c.device]) {
+    if (cudaFuncSetAttribute(f32_attention_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)smem_bytes(kMaxD)) != cudaSuccess)
+      return kErrLaunch;
+    attr_done[c.device] = 1;
+  }
+  F32Params p;
+  p.q = static_cast<const float*>(c.q);
+  p.k = static_cast<const float*>(c.k);
+  p.v = static_cast<const float*>(c.v);
+  p.out = static_cast<float*>(c.out);
+  p.T = c.T;
+  p.start_pos = c.start_pos;
+  p.L = c.start_pos + c.T;
+  p.H = c.H;
+  p.Hkv = c.Hkv;
+  p.group = c.H / c.Hkv;
+  p.D = c.D;
+  p.window = c.window;
+  p.scale_log2 = (float)((double)c.scale * 1.4426950408889634);
+  p.rows_per_head = c.T * (int64_t)p.group;
+  const int64_t bx = (p.rows_per_head + kRowsPerBlock - 1) / kRowsPerBlock;
+  if (bx > 0x7fffffff || c.Hkv > 65535) return kErrShape;
+  dim3 grid((unsigned)bx, (unsigned)c.Hkv);
+  f32_attention_kernel<<<grid, kRowsPerBlock * 32, smem, c.stream>>>(p);
+  return cudaGetLastError() == cudaSuccess ? kOk : kErrLaunch;
+}
+
+}  // namespace pfa

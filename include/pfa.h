@@ -1,0 +1,143 @@
+/*
+ * pfa.h -- C ABI of the GB300 (sm_103a) chunked causal GQA prefill-attention
+ * library (libpfa.so).
+ *
+ * The operation is one layer's self-attention for a chunk of T query tokens
+ * at absolute positions start_pos .. start_pos+T-1 against a KV cache that
+ * already holds L = start_pos + T positions, as defined on the gnosis page
+ * "Prefill attention -> GPU: handoff", section "GPU design":
+ *
+ *   - GQA: group = num_heads / num_kv_heads; query head h reads kv head
+ *     h / group (integer division).
+ *   - scores s_j = scale * <q[t][h][:], k[h/group][j][:]>, scaled before the
+ *     row maximum and softmax (scale is usually 1/sqrt(head_dim)).
+ *   - causal mask: key j is visible to token t only if j <= start_pos + t
+ *     (masked scores contribute exactly zero weight).
+ *   - sliding window (the "causal(+windowed)" per-row [lo, hi] band of the
+ *     TensorSharp2 Gemma-4 prefill design, section 5 Option A): when
+ *     window > 0, key j is also required to satisfy j > start_pos + t - window,
+ *     so a row sees min(pos + 1, window) keys, its own position included.
+ *   - out[t][h][:] = sum_j softmax(s)_j * v[h/group][j][:].
+ *
+ * Every row has at least one visible key (its own position), so no row is
+ * ever empty.
+ */
+#ifndef PFA_H
+#define PFA_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define PFA_API __attribute__((visibility("default")))
+#else
+#define PFA_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Element type of q, k_cache, v_cache and out (all four share it). */
+typedef enum {
+    PFA_F32 = 0,   /* fp32 in, fp32 out, fp32 arithmetic throughout          */
+    PFA_BF16 = 1   /* bf16 in, bf16 out (round-to-nearest-even), fp32 accumulation */
+} pfa_dtype;
+
+/* Status codes.  Every entry point returns one of these and never aborts,
+ * traps or prints (unless the environment variable PFA_TRACE is set, which
+ * makes the launch path print one line per call to stderr). */
+typedef enum {
+    PFA_OK = 0,
+    PFA_ERR_NULL = -1,       /* a required pointer is NULL                          */
+    PFA_ERR_SHAPE = -2,      /* T < 0, start_pos < 0, heads <= 0, H % Hkv != 0,
+                                unsupported head_dim, or a size beyond the limits   */
+    PFA_ERR_DTYPE = -3,      /* dtype is not a pfa_dtype value                      */
+    PFA_ERR_ALIGNMENT = -4,  /* a pointer is not 16-byte aligned                    */
+    PFA_ERR_DEVICE = -5,     /* no usable device, or not an sm_103 (GB300) device,
+                                or a pointer that is not device-accessible memory   */
+    PFA_ERR_LAUNCH = -6,     /* the CUDA runtime refused the launch                 */
+    PFA_ERR_TIMEOUT = -7,    /* a device-side wait gave up (reported after a sync
+                                by pfa_last_device_error)                           */
+    PFA_ERR_VALUE = -8,      /* scale is not a finite number                        */
+    PFA_ERR_ALIAS = -9       /* out overlaps q, k_cache or v_cache                  */
+} pfa_status;
+
+/*
+ * pfa_prefill_attention -- asynchronous prefill attention on `stream`.
+ *
+ *   q        device pointer, [T][num_heads][head_dim] contiguous, dtype.
+ *            Token-major, as the page's batch_q rows (section "GPU design",
+ *            "Layout").
+ *   k_cache  device pointer, [num_kv_heads][L][head_dim] contiguous, dtype,
+ *            L = start_pos + T: each kv head's keys form one contiguous
+ *            [L x head_dim] block (the page's kv_cache.keys layout with
+ *            capacity L).  Positions start_pos .. L-1 must already hold the
+ *            chunk's own keys.
+ *   v_cache  device pointer, same layout as k_cache.
+ *   out      device pointer, [T][num_heads][head_dim] contiguous, dtype.  It
+ *            must not overlap q, k_cache or v_cache.  Every element is
+ *            written.
+ *   T        number of query tokens in the chunk (T == 0 is a no-op).
+ *   start_pos  absolute position of the chunk's first token (>= 0).
+ *   num_heads, num_kv_heads  query and kv head counts; num_heads must be a
+ *            multiple of num_kv_heads.  For PFA_BF16 the group size
+ *            num_heads / num_kv_heads must be at most 128.
+ *   head_dim 128 or 512 for PFA_BF16; any multiple of 4 up to 512 for PFA_F32.
+ *   window   <= 0: global causal attention; > 0: sliding window of that many
+ *            keys (key j visible iff start_pos+t-window < j <= start_pos+t).
+ *   scale    multiplier of the dot products, applied as given (finite).
+ *   dtype    a pfa_dtype value.
+ *   stream   cudaStream_t to launch on; NULL means the legacy default stream.
+ *
+ * Ownership: the caller owns all four buffers and keeps them alive until the
+ * work on `stream` completes.  The library allocates no device memory for
+ * this call; it caches TMA tensor-map descriptors (host memory) keyed by
+ * pointer and shape, and per-device launch attributes.
+ *
+ * Behaviour: validates the arguments, then enqueues the kernel(s) on `stream`
+ * and returns without synchronising.  Validation failures return a status
+ * before anything is enqueued.  A device-side wait that exceeds its time
+ * limit makes the kernel record PFA_ERR_TIMEOUT and return early; read it
+ * with pfa_last_device_error.  The result is a deterministic function of the
+ * inputs: repeated calls produce bit-identical outputs.
+ *
+ * Returns PFA_OK or a pfa_status error code.
+ */
+PFA_API int pfa_prefill_attention(const void *q, const void *k_cache, const void *v_cache, void *out,
+                          int64_t T, int64_t start_pos, int num_heads, int num_kv_heads,
+                          int head_dim, int window, float scale, int dtype, void *stream);
+
+/* Human-readable name of a pfa_status value (static storage, never NULL). */
+PFA_API const char *pfa_status_string(int status);
+
+/*
+ * pfa_last_device_error -- synchronise `stream`, then return and clear the
+ * device-side error word of the current device: PFA_OK, or PFA_ERR_TIMEOUT if
+ * a kernel launched since the last call gave up on a wait.  Returns
+ * PFA_ERR_DEVICE if the stream cannot be synchronised (the CUDA error is then
+ * the runtime's).
+ */
+PFA_API int pfa_last_device_error(void *stream);
+
+/* Library ABI version: (major << 16) | minor. */
+PFA_API int pfa_version(void);
+
+/*
+ * pfa_debug_configure -- test hook for the device-side wait limits.
+ *   wait_limit_ms  time limit of every device-side wait in later launches
+ *                  (<= 0 restores the default of 2000 ms).
+ *   force_timeout  non-zero makes the next bf16 launches wait once on a
+ *                  barrier that nothing signals, so the limit expires and the
+ *                  kernel takes its early-exit path (PFA_ERR_TIMEOUT);
+ *                  zero restores normal operation.
+ * Process-wide setting; not thread-safe with concurrent launches.
+ * Returns PFA_OK.
+ */
+PFA_API int pfa_debug_configure(double wait_limit_ms, int force_timeout);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* PFA_H */

@@ -1,0 +1,91 @@
+"""The C-ABI library: builds, loads, exports every declared symbol, and
+rejects bad arguments before touching a GPU (no compute calls here)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import chunked_causal_gqa_gb300 as pkg
+from chunked_causal_gqa_gb300 import _binding, build
+
+HEADER = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))),
+                      "include", "pfa.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    build.build()
+    return _binding.load()
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    return sorted(set(re.findall(r"PFA_API\s+[\w\s\*]*?\b(pfa_\w+)\s*\(", text)))
+
+
+def test_header_declares_the_binding_exports():
+    assert declared_functions() == sorted(_binding.EXPORTS)
+
+
+def test_library_exports_every_declared_symbol(lib):
+    for name in declared_functions():
+        assert hasattr(lib, name), name
+
+
+def test_status_strings(lib):
+    for code, name in _binding.STATUS.items():
+        assert lib.pfa_status_string(code).decode().startswith(name)
+    assert lib.pfa_status_string(12345)
+
+
+def test_version(lib):
+    assert pkg.version()[0] == 1
+
+
+BF16, F32 = _binding.PFA_BF16, _binding.PFA_F32
+A, B, C, O = 0x10000, 0x20000000, 0x40000000, 0x60000000   # aligned, disjoint fake pointers
+
+
+def call(lib, q=A, k=B, v=C, o=O, T=16, sp=0, H=8, Hkv=2, D=128, w=0, scale=0.1, dt=BF16):
+    return lib.pfa_prefill_attention(q, k, v, o, T, sp, H, Hkv, D, w, scale, dt, None)
+
+
+def test_argument_validation_without_gpu(lib):
+    assert call(lib, dt=7) == -3                       # dtype
+    assert call(lib, T=-1) == -2                       # shape
+    assert call(lib, sp=-3) == -2
+    assert call(lib, H=6, Hkv=4) == -2                 # H % Hkv
+    assert call(lib, H=0) == -2
+    assert call(lib, D=96) == -2                       # bf16 head_dim
+    assert call(lib, D=130, dt=F32) == -2              # fp32 head_dim not a multiple of 4
+    assert call(lib, D=516, dt=F32) == -2
+    assert call(lib, H=256, Hkv=1) == -2               # bf16 group > 128
+    assert call(lib, scale=float("nan")) == -8
+    assert call(lib, scale=float("inf")) == -8
+    assert call(lib, T=0, q=None, k=None, v=None, o=None) == 0   # empty chunk: no-op
+    assert call(lib, q=None) == -1
+    assert call(lib, o=None) == -1
+    assert call(lib, k=B + 8) == -4                    # alignment
+    assert call(lib, o=A + 64) == -9                   # out overlaps q
+    assert call(lib, o=B + 4096) == -9                 # out overlaps k_cache
+
+
+def test_valid_arguments_reach_the_device_check(lib):
+    import torch
+    if torch.cuda.is_available():
+        pytest.skip("a GPU is present: covered by the gpu tests")
+    assert call(lib) == -5
+    assert call(lib, D=100, dt=F32) == -5
+
+
+def test_python_binding_checks_tensors():
+    import torch
+    q = torch.zeros(4, 8, 128, dtype=torch.bfloat16)
+    k = torch.zeros(2, 4, 128, dtype=torch.bfloat16)
+    with pytest.raises(ValueError):
+        pkg.prefill_attention(q, k, k.float())
+    with pytest.raises(ValueError):
+        pkg.prefill_attention(q, k[:, :3], k[:, :3])
+    with pytest.raises(ValueError):
+        pkg.prefill_attention(q[0], k, k)

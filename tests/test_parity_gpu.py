@@ -1,0 +1,178 @@
+"""The CUDA path (through the C ABI) against the fp64 oracle.
+
+Small cases compare every output element; the full-size 64k/128k chunks
+compare sampled rows that the oracle computes one by one.  Tolerances are the
+ones stated for the two dtypes (fp32: max |err| <= 1e-4; bf16 inputs with fp32
+accumulation: |err| <= 2e-2 + 1e-2 |oracle|).
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from chunked_causal_gqa_gb300 import workloads as W
+from tests import gpu_util as G
+
+pytestmark = pytest.mark.gpu
+
+
+# (H, Hkv, D, T, start_pos, window): tiles of 128 rows (group heads x 128/group
+# tokens), key tiles of 128, ragged tails, every supported group-size regime.
+BF16_CASES = [
+    (32, 8, 128, 300, 200, 0),     # Mistral-like GQA 4, ragged T and L
+    (8, 2, 128, 257, 0, 0),        # prompt from position 0, one token past a tile
+    (8, 2, 128, 64, 1000, 0),      # short chunk deep in the cache
+    (4, 4, 128, 130, 5, 0),        # group 1: 128 tokens per tile
+    (16, 8, 128, 200, 33, 0),      # group 2
+    (16, 2, 128, 100, 50, 0),      # group 8
+    (6, 2, 128, 150, 20, 0),       # group 3: 126-row tiles
+    (32, 1, 128, 40, 10, 0),       # group 32: 4 tokens per tile
+    (128, 1, 128, 5, 3, 0),        # group 128: 1 token per tile
+    (8, 2, 128, 300, 500, 100),    # window inside one key tile
+    (8, 2, 128, 300, 500, 129),    # window band crossing key tiles
+    (8, 2, 128, 200, 0, 1000),     # window longer than the prompt
+    (8, 2, 128, 1, 0, 0),          # a single first token
+    (8, 2, 128, 1, 777, 0),        # a single token deep in the cache
+]
+
+
+@pytest.mark.parametrize("case", BF16_CASES, ids=lambda c: "H%d_Hkv%d_D%d_T%d_sp%d_w%d" % c)
+def test_bf16_small_full_parity(case):
+    H, Hkv, D, T, sp, w = case
+    q, k, v = W.make_random(T, sp, H, Hkv, D, "bf16", seed=sum(case), q_std=1.0, kv_std=0.5)
+    got = G.to_np(G.run(q, k, v, window=w))
+    want = oracle.prefill_attention(q, k, v, window=w)
+    G.check(got, want, "bf16", str(case))
+
+
+F32_CASES = [
+    (8, 2, 64, 77, 30, 0),
+    (4, 1, 100, 50, 10, 7),
+    (8, 2, 512, 33, 20, 0),
+    (6, 3, 36, 40, 0, 5),
+    (2, 2, 128, 1, 100, 0),
+]
+
+
+@pytest.mark.parametrize("case", F32_CASES, ids=lambda c: "H%d_Hkv%d_D%d_T%d_sp%d_w%d" % c)
+def test_f32_small_full_parity(case):
+    H, Hkv, D, T, sp, w = case
+    q, k, v = W.make_random(T, sp, H, Hkv, D, "f32", seed=sum(case))
+    got = G.to_np(G.run(q, k, v, window=w))
+    want = oracle.prefill_attention(q, k, v, window=w)
+    G.check(got, want, "f32", str(case))
+
+
+def test_tiny_f32_workload_full_parity():
+    wl = W.WORKLOADS["tiny_f32"]
+    q, k, v = W.make_inputs(wl)
+    got = G.to_np(G.run(q, k, v, window=wl.window, scale=wl.scale))
+    want = oracle.prefill_attention(q, k, v, window=wl.window, scale=wl.scale)
+    G.check(got, want, "f32", wl.name)
+
+
+def test_mistral_layer_full_parity():
+    wl = W.WORKLOADS["mistral_1358"]
+    q, k, v = W.make_inputs(wl)
+    got = G.to_np(G.run(q, k, v, window=wl.window, scale=wl.scale))
+    want = oracle.prefill_attention(q, k, v, window=wl.window, scale=wl.scale)
+    G.check(got, want, "bf16", wl.name)
+
+
+@pytest.mark.parametrize("name", ["chunk_64k", "chunk_128k"])
+def test_long_chunk_sampled_parity(name):
+    wl = W.WORKLOADS[name]
+    q, k, v = W.make_inputs(wl)
+    out = G.run(q, k, v, window=wl.window, scale=wl.scale)
+    rows = G.sample_rows(wl.T, wl.num_heads, 24, seed=wl.seeds[0])
+    want = oracle.prefill_attention_rows(q, k, v, rows, window=wl.window, scale=wl.scale)
+    got = G.to_np(out)[[t for t, _ in rows], [h for _, h in rows]]
+    G.check(got, want, "bf16", name)
+    assert torch.isfinite(out.float()).all()
+
+
+def test_repeated_runs_are_bit_identical():
+    wl = W.WORKLOADS["mistral_1358"]
+    q, k, v = (x.to(G.dev()) for x in W.make_inputs(wl))
+    digests = {G.digest(G.run(q, k, v, scale=wl.scale)) for _ in range(5)}
+    assert len(digests) == 1
+
+
+@pytest.mark.parametrize("window", [0, 200])
+def test_chunked_prefill_equals_one_shot(window):
+    """Prefilling the second chunk against the cache gives the same rows as a
+    single prefill of the whole prompt."""
+    H, Hkv, D, T1, T2 = 32, 8, 128, 384, 300
+    q, k, v = W.make_random(T1 + T2, 0, H, Hkv, D, "bf16", seed=41, kv_std=0.5)
+    full = G.run(q, k, v, window=window)
+    chunk = G.run(q[T1:].contiguous(), k, v, window=window)
+    assert torch.equal(chunk, full[T1:])
+
+
+@pytest.mark.parametrize("window", [0, 150])
+def test_masked_keys_never_change_outputs(window):
+    H, Hkv, D, T, sp = 8, 2, 128, 256, 300
+    q, k, v = W.make_random(T, sp, H, Hkv, D, "bf16", seed=43)
+    base = G.run(q, k, v, window=window)
+    t_cut = 100
+    k2, v2 = k.clone(), v.clone()
+    k2[:, sp + t_cut + 1:] = 7.0          # keys after row t_cut's position
+    v2[:, sp + t_cut + 1:] = -3.0
+    got = G.run(q, k2, v2, window=window)
+    assert torch.equal(got[:t_cut + 1], base[:t_cut + 1])
+    if window > 0:
+        # keys at or before pos - window for every row t >= t_lo
+        t_lo = 200
+        cut = sp + t_lo - window + 1
+        k3, v3 = k.clone(), v.clone()
+        k3[:, :cut] = 5.0
+        v3[:, :cut] = 9.0
+        got = G.run(q, k3, v3, window=window)
+        assert torch.equal(got[t_lo:], base[t_lo:])
+
+
+def test_group_heads_with_equal_queries_agree():
+    H, Hkv, D, T, sp = 8, 2, 128, 100, 60
+    q, k, v = W.make_random(T, sp, H, Hkv, D, "bf16", seed=44)
+    q[:, 1] = q[:, 0]
+    q[:, 3] = q[:, 0]
+    q[:, 4] = q[:, 0]      # first head of the other group
+    out = G.run(q, k, v)
+    assert torch.equal(out[:, 0], out[:, 1])
+    assert torch.equal(out[:, 0], out[:, 3])
+    assert not torch.equal(out[:, 0], out[:, 4])
+
+
+def test_window_one_returns_own_value_row():
+    H, Hkv, D, T, sp = 8, 2, 128, 200, 90
+    q, k, v = W.make_random(T, sp, H, Hkv, D, "bf16", seed=45)
+    out = G.run(q, k, v, window=1).cpu()
+    want = torch.stack([v[h // 4, sp:sp + T] for h in range(H)], dim=1)
+    assert torch.equal(out, want)
+
+
+def test_out_argument_and_host_tensors():
+    H, Hkv, D, T, sp = 8, 2, 128, 70, 10
+    q, k, v = W.make_random(T, sp, H, Hkv, D, "bf16", seed=46)
+    d = G.dev()
+    out = torch.full((T, H, D), float("nan"), dtype=torch.bfloat16, device=d)
+    import chunked_causal_gqa_gb300 as pkg
+    r = pkg.prefill_attention(q.to(d), k.to(d), v.to(d), out=out)
+    assert r.data_ptr() == out.data_ptr()
+    host = pkg.prefill_attention(q, k, v)      # CPU tensors: copied in and out
+    assert host.device.type == "cpu"
+    assert torch.equal(host, out.cpu())
+
+
+def test_errors_from_the_device_path():
+    import chunked_causal_gqa_gb300 as pkg
+    d = G.dev()
+    q = torch.zeros(4, 8, 96, dtype=torch.bfloat16, device=d)
+    k = torch.zeros(2, 4, 96, dtype=torch.bfloat16, device=d)
+    with pytest.raises(pkg.PfaError) as e:
+        pkg.prefill_attention(q, k, k)
+    assert e.value.status == -2
+    q = torch.zeros(4, 8, 128, dtype=torch.bfloat16, device=d)
+    k = torch.zeros(2, 4, 128, dtype=torch.bfloat16, device=d)
+    empty = pkg.prefill_attention(q[:0], k[:, :0], k[:, :0])
+    assert empty.shape == (0, 8, 128)
