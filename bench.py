@@ -241,9 +241,13 @@ def run_ours(args, wl):
     out = torch.empty_like(q)
     flush = torch.empty(256 * 1024 * 1024, dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream(dev)
+    ws_bytes = pkg.workspace_bytes(wl.T, wl.start_pos, wl.num_heads, wl.num_kv_heads,
+                                   wl.head_dim, wl.window, W.torch_dtype(wl.dtype))
+    workspace = torch.empty(ws_bytes, dtype=torch.uint8, device=dev) if ws_bytes > 0 else None
 
     def step():
-        pkg.prefill_attention(q, k, v, out=out, window=wl.window, scale=wl.scale)
+        pkg.prefill_attention(q, k, v, out=out, window=wl.window, scale=wl.scale,
+                              workspace=workspace)
 
     for _ in range(args.warmup):
         flush.fill_(1)
@@ -347,7 +351,9 @@ def run_ours(args, wl):
             "frac_of_bf16_peak": value / world / float(peaks["bf16_tflops"]),
             "ms_min": min(per), "ms_median": statistics.median(per),
             "wall_s_timed": wall,
-            "gpu_launches": args.steps * launches_per_step(wl),
+            "gpu_launches": args.steps * (2 if ws_bytes > 0 else 1),
+            "schedule": "balanced" if ws_bytes > 0 else "plain",
+            "workspace_bytes": ws_bytes,
             "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e, "clocks": clocks,
         }
         print(json.dumps(line), flush=True)
@@ -356,14 +362,10 @@ def run_ours(args, wl):
     return 0
 
 
-def launches_per_step(wl) -> int:
-    return 1
-
-
 def main(argv=None):
     ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--steps", type=int, default=10000)
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default="mistral_1358")

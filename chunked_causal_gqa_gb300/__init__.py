@@ -21,7 +21,7 @@ import torch
 from . import _binding
 from ._binding import PFA_BF16, PFA_F32, PfaError
 
-__all__ = ["prefill_attention", "last_device_error", "status_string", "version",
+__all__ = ["prefill_attention", "workspace_bytes", "last_device_error", "status_string", "version",
            "debug_configure", "PfaError", "PFA_F32", "PFA_BF16"]
 
 _DTYPES = {torch.float32: PFA_F32, torch.bfloat16: PFA_BF16}
@@ -33,15 +33,34 @@ def _stream_handle(device: torch.device, stream) -> int:
     return int(stream.cuda_stream)
 
 
+def workspace_bytes(T: int, start_pos: int, num_heads: int, num_kv_heads: int, head_dim: int,
+                    window: int = 0, dtype: torch.dtype = torch.bfloat16) -> int:
+    """Workspace bytes the balanced schedule needs on the current device (0: unused)."""
+    import ctypes
+    lib = _binding.load()
+    n = ctypes.c_size_t(0)
+    rc = lib.pfa_workspace_bytes(int(T), int(start_pos), int(num_heads), int(num_kv_heads),
+                                 int(head_dim), int(window), _DTYPES[dtype], ctypes.byref(n))
+    if rc != 0:
+        raise PfaError(rc, "pfa_workspace_bytes")
+    return int(n.value)
+
+
 def prefill_attention(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor,
                       out: torch.Tensor | None = None, *, start_pos: int | None = None,
-                      window: int = 0, scale: float | None = None, stream=None) -> torch.Tensor:
-    """Chunked causal GQA prefill attention through pfa_prefill_attention.
+                      window: int = 0, scale: float | None = None, stream=None,
+                      workspace="auto") -> torch.Tensor:
+    """Chunked causal GQA prefill attention through the C ABI.
 
     q: [T, num_heads, head_dim]; k_cache, v_cache: [num_kv_heads, L, head_dim]
     with L = start_pos + T (start_pos defaults to L - T); all contiguous, of
     one dtype (float32 or bfloat16).  window <= 0 means global causal.  scale
     defaults to 1/sqrt(head_dim) rounded to float32.
+
+    workspace: "auto" (default) allocates the balanced schedule's workspace
+    from torch's caching allocator when the shape uses one
+    (pfa_prefill_attention_ws); a uint8 CUDA tensor supplies it; None runs
+    the plain schedule (pfa_prefill_attention, no workspace).
 
     CUDA tensors: the call is enqueued on `stream` (default: the current
     stream) and returns without synchronising.  CPU tensors: they are copied to
@@ -87,17 +106,34 @@ def prefill_attention(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Ten
     lib = _binding.load()
     with torch.cuda.device(dev):
         st = _stream_handle(dev, stream)
-        rc = lib.pfa_prefill_attention(qd.data_ptr(), kd.data_ptr(), vd.data_ptr(), od.data_ptr(),
-                                       int(T), int(start_pos), int(H), int(Hkv), int(D),
-                                       int(window), float(scale), _DTYPES[q.dtype], st)
+        ws_ptr, ws_bytes = None, 0
+        if isinstance(workspace, str):
+            if workspace != "auto":
+                raise ValueError("workspace must be 'auto', None or a uint8 CUDA tensor")
+            need = workspace_bytes(T, start_pos, H, Hkv, D, window, q.dtype) if T > 0 else 0
+            if need > 0:
+                workspace = torch.empty(need, dtype=torch.uint8, device=dev)
+            else:
+                workspace = None
+        if workspace is not None:
+            if workspace.device != dev or workspace.dtype != torch.uint8:
+                raise ValueError("workspace must be a uint8 tensor on the output's device")
+            ws_ptr, ws_bytes = workspace.data_ptr(), workspace.numel()
+        rc = lib.pfa_prefill_attention_ws(qd.data_ptr(), kd.data_ptr(), vd.data_ptr(),
+                                          od.data_ptr(), int(T), int(start_pos), int(H), int(Hkv),
+                                          int(D), int(window), float(scale), _DTYPES[q.dtype],
+                                          ws_ptr, ws_bytes, st)
+        if workspace is not None and stream is not None:
+            # the caching allocator must not hand the workspace out again
+            # before the work on `stream` is done
+            workspace.record_stream(stream)
     if rc != 0:
         raise PfaError(rc, "pfa_prefill_attention")
     if host:
-        res = od.to("cpu")
         if out is not None:
-            out.copy_(res)
+            out.copy_(od)          # device -> host (synchronises)
             return out
-        return res
+        return od.to("cpu")
     return od
 
 

@@ -21,8 +21,8 @@ STATUS = {
     -4: "PFA_ERR_ALIGNMENT", -5: "PFA_ERR_DEVICE", -6: "PFA_ERR_LAUNCH",
     -7: "PFA_ERR_TIMEOUT", -8: "PFA_ERR_VALUE", -9: "PFA_ERR_ALIAS",
 }
-EXPORTS = ("pfa_prefill_attention", "pfa_status_string", "pfa_last_device_error",
-           "pfa_version", "pfa_debug_configure")
+EXPORTS = ("pfa_prefill_attention", "pfa_prefill_attention_ws", "pfa_workspace_bytes",
+           "pfa_status_string", "pfa_last_device_error", "pfa_version", "pfa_debug_configure")
 
 _lock = threading.Lock()
 _lib = None
@@ -51,6 +51,13 @@ def load(path: str | None = None) -> ctypes.CDLL:
         lib.pfa_prefill_attention.argtypes = [vp, vp, vp, vp, i64, i64, i32, i32, i32, i32,
                                               ctypes.c_float, i32, vp]
         lib.pfa_prefill_attention.restype = i32
+        sz = ctypes.c_size_t
+        lib.pfa_prefill_attention_ws.argtypes = [vp, vp, vp, vp, i64, i64, i32, i32, i32, i32,
+                                                 ctypes.c_float, i32, vp, sz, vp]
+        lib.pfa_prefill_attention_ws.restype = i32
+        lib.pfa_workspace_bytes.argtypes = [i64, i64, i32, i32, i32, i32, i32,
+                                            ctypes.POINTER(sz)]
+        lib.pfa_workspace_bytes.restype = i32
         lib.pfa_status_string.argtypes = [i32]
         lib.pfa_status_string.restype = ctypes.c_char_p
         lib.pfa_last_device_error.argtypes = [vp]

@@ -208,16 +208,20 @@ int pfa_debug_configure(double wait_limit_ms, int force_timeout) {
   return PFA_OK;
 }
 
-int pfa_prefill_attention(const void* q, const void* k_cache, const void* v_cache, void* out,
-                          int64_t T, int64_t start_pos, int num_heads, int num_kv_heads,
-                          int head_dim, int window, float scale, int dtype, void* stream) {
+namespace {
+
+// Validation shared by every entry point.  On success fills *c (without the
+// workspace) and returns PFA_OK; T == 0 returns PFA_OK with c->T == 0.
+int prepare(const void* q, const void* k_cache, const void* v_cache, void* out, int64_t T,
+            int64_t start_pos, int num_heads, int num_kv_heads, int head_dim, int window,
+            float scale, int dtype, void* stream, bool check_pointers, Call* c) {
   // ---- pure argument checks (no CUDA calls)
   if (dtype != PFA_F32 && dtype != PFA_BF16) return PFA_ERR_DTYPE;
   if (T < 0 || start_pos < 0 || num_heads <= 0 || num_kv_heads <= 0) return PFA_ERR_SHAPE;
   if (num_heads % num_kv_heads != 0) return PFA_ERR_SHAPE;
   const int group = num_heads / num_kv_heads;
   if (dtype == PFA_BF16) {
-    if (head_dim != 128) return PFA_ERR_SHAPE;
+    if (head_dim != 128 && head_dim != 512) return PFA_ERR_SHAPE;
     if (group > 128) return PFA_ERR_SHAPE;
   } else {
     if (head_dim <= 0 || head_dim > 512 || head_dim % 4 != 0) return PFA_ERR_SHAPE;
@@ -226,59 +230,116 @@ int pfa_prefill_attention(const void* q, const void* k_cache, const void* v_cach
   // TMA coordinates and launch indices are 32-bit.
   if (L > ((int64_t)1 << 31) - 4096 || T > ((int64_t)1 << 31) - 4096) return PFA_ERR_SHAPE;
   if (!std::isfinite(scale)) return PFA_ERR_VALUE;
+  c->T = T;
   if (T == 0) return PFA_OK;
-  if (!q || !k_cache || !v_cache || !out) return PFA_ERR_NULL;
-  const uintptr_t mis = reinterpret_cast<uintptr_t>(q) | reinterpret_cast<uintptr_t>(k_cache) |
-                        reinterpret_cast<uintptr_t>(v_cache) | reinterpret_cast<uintptr_t>(out);
-  if (mis & 15u) return PFA_ERR_ALIGNMENT;
-  const size_t es = dtype == PFA_F32 ? 4 : 2;
-  const size_t qo_bytes = (size_t)T * num_heads * head_dim * es;
-  const size_t kv_bytes = (size_t)num_kv_heads * (size_t)L * head_dim * es;
-  if (overlaps(out, qo_bytes, q, qo_bytes) || overlaps(out, qo_bytes, k_cache, kv_bytes) ||
-      overlaps(out, qo_bytes, v_cache, kv_bytes))
-    return PFA_ERR_ALIAS;
+  if (check_pointers) {
+    if (!q || !k_cache || !v_cache || !out) return PFA_ERR_NULL;
+    const uintptr_t mis = reinterpret_cast<uintptr_t>(q) | reinterpret_cast<uintptr_t>(k_cache) |
+                          reinterpret_cast<uintptr_t>(v_cache) | reinterpret_cast<uintptr_t>(out);
+    if (mis & 15u) return PFA_ERR_ALIGNMENT;
+    const size_t es = dtype == PFA_F32 ? 4 : 2;
+    const size_t qo_bytes = (size_t)T * num_heads * head_dim * es;
+    const size_t kv_bytes = (size_t)num_kv_heads * (size_t)L * head_dim * es;
+    if (overlaps(out, qo_bytes, q, qo_bytes) || overlaps(out, qo_bytes, k_cache, kv_bytes) ||
+        overlaps(out, qo_bytes, v_cache, kv_bytes))
+      return PFA_ERR_ALIAS;
+  }
 
   // ---- device checks
   int dev = -1;
   DeviceState* st = nullptr;
   const int ds = device_state(&dev, &st);
   if (ds != kOk) return ds;
-  if (!device_accessible(q, dev) || !device_accessible(k_cache, dev) ||
-      !device_accessible(v_cache, dev) || !device_accessible(out, dev))
+  if (check_pointers &&
+      (!device_accessible(q, dev) || !device_accessible(k_cache, dev) ||
+       !device_accessible(v_cache, dev) || !device_accessible(out, dev)))
     return PFA_ERR_DEVICE;
 
-  Call c;
-  c.q = q;
-  c.k = k_cache;
-  c.v = v_cache;
-  c.out = out;
-  c.T = T;
-  c.start_pos = start_pos;
-  c.H = num_heads;
-  c.Hkv = num_kv_heads;
-  c.D = head_dim;
-  c.window = window > 0 ? window : 0;
-  c.scale = scale;
-  c.stream = static_cast<cudaStream_t>(stream);
-  c.err = st->err;
+  c->q = q;
+  c->k = k_cache;
+  c->v = v_cache;
+  c->out = out;
+  c->start_pos = start_pos;
+  c->H = num_heads;
+  c->Hkv = num_kv_heads;
+  c->D = head_dim;
+  c->window = window > 0 ? window : 0;
+  c->scale = scale;
+  c->stream = static_cast<cudaStream_t>(stream);
+  c->err = st->err;
   {
     std::lock_guard<std::mutex> lk(g_mutex);
-    c.wait_limit_ns = (uint64_t)(g_wait_limit_ms * 1e6);
-    c.flags = g_force_timeout ? kFlagForceTimeout : 0;
+    c->wait_limit_ns = (uint64_t)(g_wait_limit_ms * 1e6);
+    c->flags = g_force_timeout ? kFlagForceTimeout : 0;
   }
-  c.device = dev;
-  c.num_sms = st->num_sms;
+  c->device = dev;
+  c->num_sms = st->num_sms;
+  c->ws = nullptr;
+  c->ws_bytes = 0;
+  return PFA_OK;
+}
 
+int dispatch(const Call& c, int dtype) {
   int rc;
   if (dtype == PFA_F32)
     rc = launch_f32(c);
-  else
+  else if (c.D == 128)
     rc = launch_bf16_d128(c);
+  else
+    rc = launch_bf16_d512(c);
   if (trace_on())
-    std::fprintf(stderr, "[pfa] dtype=%d T=%lld start_pos=%lld H=%d Hkv=%d D=%d window=%d -> %d\n",
-                 dtype, (long long)T, (long long)start_pos, num_heads, num_kv_heads, head_dim,
-                 c.window, rc);
+    std::fprintf(stderr,
+                 "[pfa] dtype=%d T=%lld start_pos=%lld H=%d Hkv=%d D=%d window=%d ws=%zu -> %d\n",
+                 dtype, (long long)c.T, (long long)c.start_pos, c.H, c.Hkv, c.D, c.window,
+                 c.ws_bytes, rc);
   return rc;
+}
+
+}  // namespace
+
+int pfa_prefill_attention(const void* q, const void* k_cache, const void* v_cache, void* out,
+                          int64_t T, int64_t start_pos, int num_heads, int num_kv_heads,
+                          int head_dim, int window, float scale, int dtype, void* stream) {
+  return pfa_prefill_attention_ws(q, k_cache, v_cache, out, T, start_pos, num_heads,
+                                  num_kv_heads, head_dim, window, scale, dtype, nullptr, 0,
+                                  stream);
+}
+
+int pfa_prefill_attention_ws(const void* q, const void* k_cache, const void* v_cache, void* out,
+                             int64_t T, int64_t start_pos, int num_heads, int num_kv_heads,
+                             int head_dim, int window, float scale, int dtype, void* workspace,
+                             size_t workspace_bytes, void* stream) {
+  Call c;
+  const int rc = prepare(q, k_cache, v_cache, out, T, start_pos, num_heads, num_kv_heads,
+                         head_dim, window, scale, dtype, stream, true, &c);
+  if (rc != PFA_OK || c.T == 0) return rc;
+  if (workspace != nullptr && workspace_bytes > 0) {
+    if (reinterpret_cast<uintptr_t>(workspace) & 255u) return PFA_ERR_ALIGNMENT;
+    if (!device_accessible(workspace, c.device)) return PFA_ERR_DEVICE;
+    const size_t qo_bytes = (size_t)T * num_heads * head_dim * (dtype == PFA_F32 ? 4 : 2);
+    const size_t kv_bytes =
+        (size_t)num_kv_heads * (size_t)(start_pos + T) * head_dim * (dtype == PFA_F32 ? 4 : 2);
+    if (overlaps(workspace, workspace_bytes, out, qo_bytes) ||
+        overlaps(workspace, workspace_bytes, q, qo_bytes) ||
+        overlaps(workspace, workspace_bytes, k_cache, kv_bytes) ||
+        overlaps(workspace, workspace_bytes, v_cache, kv_bytes))
+      return PFA_ERR_ALIAS;
+    c.ws = workspace;
+    c.ws_bytes = workspace_bytes;
+  }
+  return dispatch(c, dtype);
+}
+
+int pfa_workspace_bytes(int64_t T, int64_t start_pos, int num_heads, int num_kv_heads,
+                        int head_dim, int window, int dtype, size_t* bytes) {
+  if (!bytes) return PFA_ERR_NULL;
+  *bytes = 0;
+  Call c;
+  const int rc = prepare(nullptr, nullptr, nullptr, nullptr, T, start_pos, num_heads,
+                         num_kv_heads, head_dim, window, 1.0f, dtype, nullptr, false, &c);
+  if (rc != PFA_OK || c.T == 0) return rc;
+  if (dtype == PFA_BF16 && head_dim == 128) *bytes = workspace_bytes_bf16_d128(c);
+  return PFA_OK;
 }
 
 int pfa_last_device_error(void* stream) {

@@ -5,17 +5,28 @@
 // steps 1-3, fused): per query row, scores against the visible keys of its kv
 // head, scale, causal (+ window) mask, softmax, weighted sum of V.
 //
-// Work unit (one CTA): one kv head and two consecutive 128-row query tiles,
-// A and B.  A tile packs all `group` query heads of the kv head for
+// Pair (the unit of query work): one kv head and two consecutive 128-row query
+// tiles, A and B.  A tile packs all `group` query heads of the kv head for
 // 128 / group consecutive tokens (row r -> token r / group, head r % group),
 // so every K/V tile that TMA brings into shared memory feeds all heads of the
 // GQA group, and both tiles.
 //
-// Warp roles (10 warps):
+// Work item: a pair and a range [kb, ke) of its key tiles.  A CTA executes a
+// list of items in order.  With the plain schedule every CTA runs one item,
+// a whole pair, and writes the normalised output.  With the balanced schedule
+// (a caller-provided workspace) the host cuts the pairs' key tiles into at
+// most one run of items per SM, of equal cost (tiles plus a fixed per-item
+// overhead); an item that covers only part of a pair writes its unnormalised
+// partial (O, exponent base, row sum) to a workspace slot, and merge_kernel
+// combines the pieces of each such pair in a fixed order (the log-sum-exp
+// identity of the softmax; the result is deterministic).
+//
+// Warp roles (12 warps, three warpgroups):
 //   warps 0-3  softmax for tile A (TMEM lanes 0-127, one row per thread)
 //   warps 4-7  softmax for tile B
-//   warp  8    TMA producer: Q tiles once, then K/V tiles into a 5-slot ring
+//   warp  8    TMA producer: Q tiles of each item, K/V tiles into a 5-slot ring
 //   warp  9    TMEM allocator and single-thread tcgen05.mma issuer
+//   warps 10-11 idle (complete the third warpgroup)
 //
 // Tensor memory (512 columns x 128 lanes, fp32 cells):
 //   [  0,128) S_A = Q_A K^T ; after softmax its first 64 columns hold P_A as
@@ -40,12 +51,21 @@
 // j <= pos and (window <= 0 or j > pos - window).  Key tiles outside every
 // row's band are never loaded; tiles fully inside every row's band skip the
 // per-element test.
+//
+// Registers: three warps share each of the SM's four register-file partitions,
+// so a thread starts with at most 168 registers.  The third warpgroup drops
+// to kRegsOther and the softmax warpgroups rise to kRegsSoftmax, which a row
+// of 128 fp32 scores plus its packed probabilities needs.
 #include "pfa_internal.h"
 #include "pfa_ptx.cuh"
 
 #include <cuda_bf16.h>
 
+#include <algorithm>
 #include <cmath>
+#include <memory>
+#include <mutex>
+#include <vector>
 
 namespace pfa {
 namespace {
@@ -55,7 +75,12 @@ constexpr int kBN = 128;                        // keys per K/V tile
 constexpr int kHalfBytes = 128 * 128;           // 128 rows x 64 bf16 (one 128-byte swizzle span)
 constexpr int kTileBytes = 2 * kHalfBytes;      // 128 rows x 128 bf16
 constexpr int kSlots = 5;                       // K/V ring depth (tiles)
-constexpr int kThreads = 320;
+constexpr int kThreads = 384;
+constexpr int kRegsLaunch = 168;   // per thread, as compiled for 384 threads
+constexpr int kRegsSoftmax = 208;  // warpgroups 0 and 1 after the split
+constexpr int kRegsOther = 80;     // warpgroup 2 after the split
+static_assert(8 * 32 * kRegsSoftmax + 4 * 32 * kRegsOther <= kThreads * kRegsLaunch,
+              "register split exceeds the CTA's pool");
 constexpr float kRescaleThreshold = 8.0f;       // log2 units
 
 constexpr int kSmemQ = 0;                                   // Q_A, Q_B
@@ -66,12 +91,14 @@ constexpr int kSmemAlloc = kSmemUsed + 1024;                // + alignment slack
 
 // barrier indices (8 bytes each, from kSmemBars)
 constexpr int kBarQ = 0;
-constexpr int kBarFull = 1;                  // kSlots
+constexpr int kBarQFree = 1;                 // Q buffers no longer read by the item's MMAs
+constexpr int kBarFull = 2;                  // kSlots
 constexpr int kBarEmpty = kBarFull + kSlots; // kSlots
 constexpr int kBarS = kBarEmpty + kSlots;    // 2 (A, B)
 constexpr int kBarP = kBarS + 2;             // 2
-constexpr int kBarO = kBarP + 2;             // 2
-constexpr int kBarDrain = kBarO + 2;
+constexpr int kBarO = kBarP + 2;             // 2: item's accumulators complete
+constexpr int kBarOFree = kBarO + 2;         // 2: item's epilogue has read O
+constexpr int kBarDrain = kBarOFree + 2;
 constexpr int kNumBars = kBarDrain + 1;
 constexpr int kOffTmemSlot = kNumBars * 8;
 constexpr int kOffAbort = kOffTmemSlot + 4;
@@ -80,8 +107,35 @@ static_assert(kOffAbort + 4 <= 256, "barrier area");
 constexpr uint32_t kIdescQK = idesc_bf16_f32(kBM, kBN, false);  // K-major Q and K
 constexpr uint32_t kIdescPV = idesc_bf16_f32(kBM, 128, true);   // V is N(=d)-contiguous
 
+// ---- schedule tables (kernel parameters)
+constexpr int kMaxCtas = 192;
+constexpr int kMaxItems = 512;
+constexpr int kMaxMerge = 256;
+constexpr int kMaxPieces = 512;
+constexpr int kPairRows = 2 * kBM;
+constexpr size_t kSlotFloats = (size_t)kPairRows * 128 + 2 * kPairRows;  // O, base, sum
+constexpr size_t kSlotBytes = kSlotFloats * sizeof(float);
+
+struct Item {
+  int pair, kb, ke, slot;  // key tiles [kb, ke) of the pair; slot < 0: whole pair, direct output
+};
+struct Sched {
+  int table;  // 0: CTA b runs pair b whole; 1: CTA c runs items [cta_first[c], cta_first[c+1])
+  int cta_first[kMaxCtas + 1];
+  Item items[kMaxItems];
+};
+struct MergeEntry {
+  int pair, first, count, pad;  // pieces slots[first .. first+count), in key order
+};
+struct MergeSched {
+  int num;
+  MergeEntry e[kMaxMerge];
+  int slots[kMaxPieces];
+};
+
 struct Params {
   __nv_bfloat16* out;
+  float* ws;  // partial slots (balanced schedule only)
   int64_t T, start_pos;
   int H, Hkv, group, tok_per_tile, window, units_per_head;
   float scale_log2;
@@ -97,19 +151,25 @@ struct Unit {
   int n;             // number of key tiles
 };
 
-__device__ __forceinline__ Unit unit_of(const Params& p, int b) {
+// Pair p -> kv head and token range; latest tokens (most keys) first.
+__host__ __device__ inline Unit unit_of(int64_t T, int64_t start_pos, int Hkv, int tok_per_tile,
+                                        int window, int units_per_head, int pidx) {
   Unit u;
-  u.kh = b % p.Hkv;
-  const int idx = p.units_per_head - 1 - b / p.Hkv;  // latest tokens (most keys) first
-  u.t0A = (int64_t)(2 * idx) * p.tok_per_tile;
-  u.t0B = u.t0A + p.tok_per_tile;
-  const int64_t t_end = min(u.t0B + p.tok_per_tile, p.T);  // exclusive, > t0A
-  const int64_t pos_lo = p.start_pos + u.t0A;
-  const int64_t pos_hi = p.start_pos + t_end - 1;
-  const int64_t kmin = p.window > 0 ? max((int64_t)0, pos_lo - p.window + 1) : 0;
+  u.kh = pidx % Hkv;
+  const int idx = units_per_head - 1 - pidx / Hkv;
+  u.t0A = (int64_t)(2 * idx) * tok_per_tile;
+  u.t0B = u.t0A + tok_per_tile;
+  const int64_t t_end = (u.t0B + tok_per_tile < T) ? u.t0B + tok_per_tile : T;  // > t0A
+  const int64_t pos_lo = start_pos + u.t0A;
+  const int64_t pos_hi = start_pos + t_end - 1;
+  int64_t kmin = 0;
+  if (window > 0) kmin = (pos_lo - window + 1 > 0) ? pos_lo - window + 1 : 0;
   u.kt_first = kmin / kBN;
   u.n = (int)(pos_hi / kBN - u.kt_first + 1);
   return u;
+}
+__device__ __forceinline__ Unit unit_of(const Params& p, int pidx) {
+  return unit_of(p.T, p.start_pos, p.Hkv, p.tok_per_tile, p.window, p.units_per_head, pidx);
 }
 
 // 8 MMAs (K = 16 each) of S = Q K^T over d = 0..127.
@@ -136,7 +196,8 @@ __device__ __forceinline__ void issue_pv(uint32_t tO, uint32_t tP, uint32_t v_ad
 template <bool kFoldScale>
 __global__ void __launch_bounds__(kThreads, 1)
 bf16_d128_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
-                 const __grid_constant__ CUtensorMap tm_v, const Params p) {
+                 const __grid_constant__ CUtensorMap tm_v, const Params p,
+                 const __grid_constant__ Sched sched) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -147,21 +208,26 @@ bf16_d128_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + kSmemBars + kOffAbort);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const Unit u = unit_of(p, blockIdx.x);
   const uint64_t lim = p.wait_limit_ns;
+  const int cta = blockIdx.x;
+  const int item_begin = sched.table ? sched.cta_first[cta] : 0;
+  const int item_end = sched.table ? sched.cta_first[cta + 1] : 1;
+  auto get_item = [&](int k) -> Item {
+    if (sched.table) return sched.items[k];
+    Item it;
+    it.pair = cta;
+    it.kb = 0;
+    it.ke = unit_of(p, cta).n;
+    it.slot = -1;
+    return it;
+  };
 
   if (threadIdx.x == 0) {
-    mbar_init(bar(kBarQ), 1);
-    for (int s = 0; s < kSlots; ++s) {
-      mbar_init(bar(kBarFull + s), 1);
-      mbar_init(bar(kBarEmpty + s), 1);
+    for (int i = 0; i < kNumBars; ++i) {
+      // P and O-free: one arrival per softmax warp; all others: one arrival
+      const bool per_warp = (i == kBarP || i == kBarP + 1 || i == kBarOFree || i == kBarOFree + 1);
+      mbar_init(bar(i), per_warp ? 4u : 1u);
     }
-    for (int x = 0; x < 2; ++x) {
-      mbar_init(bar(kBarS + x), 1);
-      mbar_init(bar(kBarP + x), 4);  // one arrival per softmax warp
-      mbar_init(bar(kBarO + x), 1);
-    }
-    mbar_init(bar(kBarDrain), 1);
     *abort_flag = 0;
     fence_mbar_init();
   }
@@ -174,94 +240,115 @@ bf16_d128_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
 
-  if (warp == 8) {
+  if (warp >= 8) {
+   regs_decrease<kRegsOther>();
+   if (warp == 8) {
     // ------------------------------------------------------------ producer
     if (lane == 0) {
       tma_prefetch_desc(&tm_q);
       tma_prefetch_desc(&tm_k);
       tma_prefetch_desc(&tm_v);
-      const int hq = u.kh * p.group;
       // Each Q box is group x tok_per_tile rows of 128 bytes (zero-filled past T).
       const uint32_t q_bytes = 4u * 128u * (uint32_t)(p.group * p.tok_per_tile);
-      mbar_arrive_expect_tx(bar(kBarQ), q_bytes);
-      tma_load_3d(sbase + kSmemQ, &tm_q, bar(kBarQ), 0, hq, (int)u.t0A);
-      tma_load_3d(sbase + kSmemQ + kHalfBytes, &tm_q, bar(kBarQ), 64, hq, (int)u.t0A);
-      tma_load_3d(sbase + kSmemQ + kTileBytes, &tm_q, bar(kBarQ), 0, hq, (int)u.t0B);
-      tma_load_3d(sbase + kSmemQ + kTileBytes + kHalfBytes, &tm_q, bar(kBarQ), 64, hq,
-                  (int)u.t0B);
-      uint32_t li = 0;
+      uint32_t li = 0, nq = 0;
       bool ok = true;
-      for (int i = 0; i < u.n && ok; ++i) {
-        const int key0 = (int)((u.kt_first + i) * kBN);
-        for (int kv = 0; kv < 2; ++kv) {
-          const uint32_t s = li % kSlots, ph = (li / kSlots) & 1u;
-          if (!mbar_wait(bar(kBarEmpty + s), ph ^ 1u, abort_flag, p.err, lim)) {
-            ok = false;
-            break;
+      for (int k = item_begin; k < item_end && ok; ++k) {
+        const Item it = get_item(k);
+        const Unit u = unit_of(p, it.pair);
+        if (nq > 0 && !(ok = mbar_wait(bar(kBarQFree), (nq - 1) & 1u, abort_flag, p.err, lim)))
+          break;
+        const int hq = u.kh * p.group;
+        mbar_arrive_expect_tx(bar(kBarQ), q_bytes);
+        tma_load_3d(sbase + kSmemQ, &tm_q, bar(kBarQ), 0, hq, (int)u.t0A);
+        tma_load_3d(sbase + kSmemQ + kHalfBytes, &tm_q, bar(kBarQ), 64, hq, (int)u.t0A);
+        tma_load_3d(sbase + kSmemQ + kTileBytes, &tm_q, bar(kBarQ), 0, hq, (int)u.t0B);
+        tma_load_3d(sbase + kSmemQ + kTileBytes + kHalfBytes, &tm_q, bar(kBarQ), 64, hq,
+                    (int)u.t0B);
+        ++nq;
+        for (int i = it.kb; i < it.ke && ok; ++i) {
+          const int key0 = (int)((u.kt_first + i) * kBN);
+          for (int kv = 0; kv < 2; ++kv) {
+            const uint32_t s = li % kSlots, ph = (li / kSlots) & 1u;
+            if (!(ok = mbar_wait(bar(kBarEmpty + s), ph ^ 1u, abort_flag, p.err, lim))) break;
+            const uint32_t dst = sbase + kSmemRing + s * kTileBytes;
+            const CUtensorMap* map = kv ? &tm_v : &tm_k;
+            mbar_arrive_expect_tx(bar(kBarFull + s), kTileBytes);
+            tma_load_3d(dst, map, bar(kBarFull + s), 0, key0, u.kh);
+            tma_load_3d(dst + kHalfBytes, map, bar(kBarFull + s), 64, key0, u.kh);
+            ++li;
           }
-          const uint32_t dst = sbase + kSmemRing + s * kTileBytes;
-          const CUtensorMap* map = kv ? &tm_v : &tm_k;
-          mbar_arrive_expect_tx(bar(kBarFull + s), kTileBytes);
-          tma_load_3d(dst, map, bar(kBarFull + s), 0, key0, u.kh);
-          tma_load_3d(dst + kHalfBytes, map, bar(kBarFull + s), 64, key0, u.kh);
-          ++li;
         }
       }
-      (void)ok;
       // No copy may be in flight when the CTA exits.  On the normal path the
       // MMA thread has already consumed every load, so these return at once.
-      mbar_wait(bar(kBarQ), 0, abort_flag, p.err, lim, true);
+      if (nq > 0) mbar_wait(bar(kBarQ), (nq - 1) & 1u, abort_flag, p.err, lim, true);
       const uint32_t first = li > (uint32_t)kSlots ? li - kSlots : 0;
       for (uint32_t j = first; j < li; ++j)
         mbar_wait(bar(kBarFull + j % kSlots), (j / kSlots) & 1u, abort_flag, p.err, lim, true);
     }
-  } else if (warp == 9) {
+   } else if (warp == 9) {
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
       const uint32_t tSA = tmem + 0, tSB = tmem + 128, tOA = tmem + 256, tOB = tmem + 384;
       const uint32_t qA = sbase + kSmemQ, qB = sbase + kSmemQ + kTileBytes;
-      bool ok = mbar_wait(bar(kBarQ), 0, abort_flag, p.err, lim);
-      tc_fence_after();
-      uint32_t li = 0;  // ring index of K_i
-      bool issued = false;
-      for (int i = 0; i < u.n && ok; ++i) {
-        const uint32_t ks = li % kSlots;
-        if (!(ok = mbar_wait(bar(kBarFull + ks), (li / kSlots) & 1u, abort_flag, p.err, lim)))
-          break;
+      uint32_t li = 0;  // ring index of the next K tile
+      uint32_t gi = 0;  // key tiles done by this CTA (phase of the S and P barriers)
+      uint32_t kk = 0;  // items done
+      bool ok = true, issued = false;
+      // O_X of the previous item must have been read by its epilogue before
+      // the first P V product of the next item overwrites it.
+      auto wait_o_free = [&](int X, int local_tile) -> bool {
+        if (local_tile != 0 || kk == 0) return true;
+        return mbar_wait(bar(kBarOFree + X), (kk - 1) & 1u, abort_flag, p.err, lim);
+      };
+      for (int k = item_begin; k < item_end && ok; ++k) {
+        const Item it = get_item(k);
+        const int n = it.ke - it.kb;
+        if (!(ok = mbar_wait(bar(kBarQ), kk & 1u, abort_flag, p.err, lim))) break;
         tc_fence_after();
-        const uint32_t k_addr = sbase + kSmemRing + ks * kTileBytes;
-        issue_qk(tSA, qA, k_addr);
-        issued = true;
-        tc_commit(bar(kBarS + 0));
-        if (i > 0) {
-          if (!(ok = mbar_wait(bar(kBarP + 1), (uint32_t)(i - 1) & 1u, abort_flag, p.err, lim)))
+        for (int i = 0; i < n; ++i) {
+          const uint32_t ks = li % kSlots;
+          if (!(ok = mbar_wait(bar(kBarFull + ks), (li / kSlots) & 1u, abort_flag, p.err, lim)))
             break;
           tc_fence_after();
-          const uint32_t vs = (li - 1) % kSlots;  // V_{i-1}
-          issue_pv(tOB, tSB, sbase + kSmemRing + vs * kTileBytes, i - 1 > 0);
-          tc_commit(bar(kBarEmpty + vs));
-        }
-        issue_qk(tSB, qB, k_addr);
-        tc_commit(bar(kBarS + 1));
-        tc_commit(bar(kBarEmpty + ks));
-        const uint32_t vs = (li + 1) % kSlots;  // V_i
-        if (!(ok = mbar_wait(bar(kBarFull + vs), ((li + 1) / kSlots) & 1u, abort_flag, p.err, lim)))
-          break;
-        if (!(ok = mbar_wait(bar(kBarP + 0), (uint32_t)i & 1u, abort_flag, p.err, lim))) break;
-        tc_fence_after();
-        issue_pv(tOA, tSA, sbase + kSmemRing + vs * kTileBytes, i > 0);
-        li += 2;
-      }
-      if (ok) {
-        ok = mbar_wait(bar(kBarP + 1), (uint32_t)(u.n - 1) & 1u, abort_flag, p.err, lim);
-        if (ok) {
+          const uint32_t k_addr = sbase + kSmemRing + ks * kTileBytes;
+          issue_qk(tSA, qA, k_addr);
+          issued = true;
+          tc_commit(bar(kBarS + 0));
+          if (i > 0) {
+            if (!(ok = mbar_wait(bar(kBarP + 1), (gi - 1) & 1u, abort_flag, p.err, lim))) break;
+            if (!(ok = wait_o_free(1, i - 1))) break;
+            tc_fence_after();
+            const uint32_t vs = (li - 1) % kSlots;  // V_{i-1}
+            issue_pv(tOB, tSB, sbase + kSmemRing + vs * kTileBytes, i - 1 > 0);
+            tc_commit(bar(kBarEmpty + vs));
+          }
+          issue_qk(tSB, qB, k_addr);
+          tc_commit(bar(kBarS + 1));
+          tc_commit(bar(kBarEmpty + ks));
+          if (i == n - 1) tc_commit(bar(kBarQFree));
+          const uint32_t vs = (li + 1) % kSlots;  // V_i
+          if (!(ok = mbar_wait(bar(kBarFull + vs), ((li + 1) / kSlots) & 1u, abort_flag, p.err,
+                               lim)))
+            break;
+          if (!(ok = mbar_wait(bar(kBarP + 0), gi & 1u, abort_flag, p.err, lim))) break;
+          if (!(ok = wait_o_free(0, i))) break;
           tc_fence_after();
-          const uint32_t vs = (li - 1) % kSlots;
-          issue_pv(tOB, tSB, sbase + kSmemRing + vs * kTileBytes, u.n - 1 > 0);
-          tc_commit(bar(kBarEmpty + vs));
-          tc_commit(bar(kBarO + 0));
-          tc_commit(bar(kBarO + 1));
+          issue_pv(tOA, tSA, sbase + kSmemRing + vs * kTileBytes, i > 0);
+          li += 2;
+          ++gi;
         }
+        if (!ok) break;
+        // last product of tile B
+        if (!(ok = mbar_wait(bar(kBarP + 1), (gi - 1) & 1u, abort_flag, p.err, lim))) break;
+        if (!(ok = wait_o_free(1, n - 1))) break;
+        tc_fence_after();
+        const uint32_t vs = (li - 1) % kSlots;
+        issue_pv(tOB, tSB, sbase + kSmemRing + vs * kTileBytes, n - 1 > 0);
+        tc_commit(bar(kBarEmpty + vs));
+        tc_commit(bar(kBarO + 0));
+        tc_commit(bar(kBarO + 1));
+        ++kk;
       }
       if (issued) {
         // Everything issued must complete before TMEM is freed (this matters
@@ -270,158 +357,181 @@ bf16_d128_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
         mbar_wait(bar(kBarDrain), 0, abort_flag, p.err, lim, true);
       }
     }
+   }
   } else {
+    regs_increase<kRegsSoftmax>();
     // ------------------------------------------------------------ softmax
     const int X = warp >> 2;        // 0: tile A, 1: tile B
     const int wq = warp & 3;        // lane quarter
     const int row = wq * 32 + lane;
-    const int64_t t0 = X ? u.t0B : u.t0A;
     const int tok = row / p.group;
     const bool row_exists = tok < p.tok_per_tile;
-    const int64_t t = t0 + tok;
-    const bool row_valid = row_exists && t < p.T;
-    const int64_t pos = p.start_pos + t;
-    const int h = u.kh * p.group + row % p.group;
-    const int64_t pos_first = p.start_pos + t0;
-    const int64_t pos_last = pos_first + p.tok_per_tile - 1;
+    const int hrow = row % p.group;
     const uint32_t lane_off = (uint32_t)(wq * 32) << 16;
     const uint32_t tS = tmem + lane_off + (uint32_t)(X * 128);
     const uint32_t tO = tmem + lane_off + 256u + (uint32_t)(X * 128);
     const float c = p.scale_log2;
 
-    float m_run = -INFINITY, l = 0.f;
     bool ok = true;
     if ((p.flags & kFlagForceTimeout) && X == 0) {
       // Test hook: wait on a barrier nothing signals, so the limit expires.
       ok = mbar_wait(bar(kBarDrain), 0, abort_flag, p.err, lim);
       ok = __all_sync(0xffffffffu, ok);
     }
-    for (int i = 0; i < u.n && ok; ++i) {
-      ok = mbar_wait(bar(kBarS + X), (uint32_t)i & 1u, abort_flag, p.err, lim);
+    uint32_t gi = 0, kk = 0;
+    for (int k = item_begin; k < item_end && ok; ++k, ++kk) {
+      const Item it = get_item(k);
+      const Unit u = unit_of(p, it.pair);
+      const int n = it.ke - it.kb;
+      // Positions and key indices fit in 32 bits (L < 2^31 - 4096).
+      const int t0 = (int)(X ? u.t0B : u.t0A);
+      const int pos_first = (int)p.start_pos + t0;
+      // first key of this item's first tile, relative to the row's position
+      int key_rel = (int)(u.kt_first + it.kb) * kBN - (pos_first + tok);
+
+      float m_run = -INFINITY, l = 0.f;
+      for (int i = 0; i < n; ++i, ++gi, key_rel += kBN) {
+        ok = mbar_wait(bar(kBarS + X), gi & 1u, abort_flag, p.err, lim);
+        if (!(ok = __all_sync(0xffffffffu, ok))) break;
+        tc_fence_after();
+
+        uint32_t r0[32], r1[32], r2[32], r3[32];  // four loads in flight
+        tmem_ld32(tS + 0, r0);
+        tmem_ld32(tS + 32, r1);
+        tmem_ld32(tS + 64, r2);
+        tmem_ld32(tS + 96, r3);
+        tmem_wait_ld(r0);
+        tmem_wait_ld(r1);
+        tmem_wait_ld(r2);
+        tmem_wait_ld(r3);
+        float x[128];
+#pragma unroll
+        for (int j = 0; j < 32; ++j) {
+          x[j] = __uint_as_float(r0[j]);
+          x[32 + j] = __uint_as_float(r1[j]);
+          x[64 + j] = __uint_as_float(r2[j]);
+          x[96 + j] = __uint_as_float(r3[j]);
+        }
+        if (!kFoldScale) {
+#pragma unroll
+          for (int j = 0; j < 128; ++j) x[j] *= c;
+        }
+        // Per-element mask unless the tile is visible to every row of the tile.
+        const int key0_minus_first = key_rel + tok;  // key0 - pos_first
+        const bool all_visible =
+            (key0_minus_first + kBN - 1 <= 0) &&
+            (p.window <= 0 || key0_minus_first > p.tok_per_tile - 1 - p.window);
+        if (!all_visible) {
+          const int hi = -key_rel;                                   // j - key0 <= pos - key0
+          const int lo = p.window > 0 ? -key_rel - p.window : -1;    // j - key0 > lo
+#pragma unroll
+          for (int j = 0; j < 128; ++j)
+            if (j > hi || j <= lo) x[j] = -INFINITY;
+        }
+        //@@MAX_BEGIN
+        float mx = -INFINITY;
+#pragma unroll
+        for (int j = 0; j < 128; ++j) mx = fmaxf(mx, x[j]);
+        //@@MAX_END
+        if (kFoldScale) mx *= c;
+
+        // Raise the exponent base only when the new maximum exceeds it by > 2^8.
+        float alpha = 1.f;
+        bool rescale = false;
+        if (mx > m_run + kRescaleThreshold) {
+          alpha = ex2(m_run - mx);  // 0 while nothing was accumulated
+          rescale = (i > 0) && (m_run != -INFINITY);
+          m_run = mx;
+        }
+        const float base = (m_run == -INFINITY) ? 0.f : m_run;
+
+        // P = 2^(s - base) as packed bf16 pairs; l gains the sum of the rounded values.
+        uint32_t pk0[32], pk1[32];
+        //@@EXP_BEGIN
+        float lsum = 0.f;
+#pragma unroll
+        for (int j = 0; j < 64; ++j) {
+          const float xa = x[2 * j], xb = x[2 * j + 1];
+          const float pa = kFoldScale ? ex2(fmaf(xa, c, -base)) : ex2(xa - base);
+          const float pb = kFoldScale ? ex2(fmaf(xb, c, -base)) : ex2(xb - base);
+          const uint32_t w = pack_bf16x2(pa, pb);
+          if (j < 32) pk0[j] = w; else pk1[j - 32] = w;
+          lsum += bf16_lo(w) + bf16_hi(w);
+        }
+        //@@EXP_END
+        l = l * alpha + lsum;
+
+        // O_X is stable here: the commit that signalled S_X(i) covers P_X(i-1) V.
+        if (__any_sync(0xffffffffu, rescale)) {
+          const float f = rescale ? alpha : 1.f;
+#pragma unroll 1
+          for (int c0 = 0; c0 < 128; c0 += 32) {
+            uint32_t o[32];
+            tmem_ld32(tO + c0, o);
+            tmem_wait_ld(o);
+#pragma unroll
+            for (int j = 0; j < 32; ++j) o[j] = __float_as_uint(__uint_as_float(o[j]) * f);
+            tmem_st32(tO + c0, o);
+          }
+        }
+        tmem_st32(tS + 0, pk0);
+        tmem_st32(tS + 32, pk1);
+        tmem_wait_st();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar(kBarP + X));
+      }
+      if (!ok) break;
+
+      ok = mbar_wait(bar(kBarO + X), kk & 1u, abort_flag, p.err, lim);
       if (!(ok = __all_sync(0xffffffffu, ok))) break;
       tc_fence_after();
-
-      uint32_t r0[32], r1[32], r2[32], r3[32];
-      tmem_ld32(tS + 0, r0);
-      tmem_ld32(tS + 32, r1);
-      tmem_ld32(tS + 64, r2);
-      tmem_ld32(tS + 96, r3);
-      tmem_wait_ld(r0);
-      tmem_wait_ld(r1);
-      tmem_wait_ld(r2);
-      tmem_wait_ld(r3);
-      float x[128];
+      const int64_t t = (int64_t)t0 + tok;
+      const bool row_valid = row_exists && t < p.T;
+      const int h = u.kh * p.group + hrow;
+      if (it.slot < 0) {
+        // whole pair: normalise, round to bf16, store token-major
+        const float inv = l > 0.f ? 1.f / l : 0.f;
+        __nv_bfloat16* orow = p.out + ((t * p.H + h) * (int64_t)128);
+#pragma unroll 1
+        for (int c0 = 0; c0 < 128; c0 += 32) {
+          uint32_t o[32];
+          tmem_ld32(tO + c0, o);
+          tmem_wait_ld(o);
+          uint32_t w[16];
 #pragma unroll
-      for (int j = 0; j < 32; ++j) {
-        x[j] = __uint_as_float(r0[j]);
-        x[32 + j] = __uint_as_float(r1[j]);
-        x[64 + j] = __uint_as_float(r2[j]);
-        x[96 + j] = __uint_as_float(r3[j]);
-      }
-      if (!kFoldScale) {
+          for (int j = 0; j < 16; ++j)
+            w[j] = pack_bf16x2(__uint_as_float(o[2 * j]) * inv, __uint_as_float(o[2 * j + 1]) * inv);
+          if (row_valid) {
+            uint4* dst = reinterpret_cast<uint4*>(orow + c0);
 #pragma unroll
-        for (int j = 0; j < 128; ++j) x[j] *= c;
-      }
-      const int64_t key0 = (u.kt_first + i) * kBN;
-      const bool all_visible = (key0 + kBN - 1 <= pos_first) &&
-                               (p.window <= 0 || key0 > pos_last - p.window);
-      if (!all_visible) {
-        const int64_t hi = pos - key0;                                   // j - key0 <= hi
-        const int64_t lo = p.window > 0 ? pos - p.window - key0 : -1;    // j - key0 > lo
-#pragma unroll
-        for (int j = 0; j < 128; ++j)
-          if (j > hi || j <= lo) x[j] = -INFINITY;
-      }
-      float mx = -INFINITY;
-#pragma unroll
-      for (int j = 0; j < 128; ++j) mx = fmaxf(mx, x[j]);
-      if (kFoldScale) mx *= c;
-
-      // Raise the exponent base only when the new maximum exceeds it by > 2^8.
-      float alpha = 1.f;
-      bool rescale = false;
-      if (mx > m_run + kRescaleThreshold) {
-        alpha = ex2(m_run - mx);  // 0 while nothing was accumulated
-        rescale = (i > 0) && (m_run != -INFINITY);
-        m_run = mx;
-      }
-      const float base = (m_run == -INFINITY) ? 0.f : m_run;
-
-      uint32_t pk0[32], pk1[32];
-      float lsum = 0.f;
-#pragma unroll
-      for (int j = 0; j < 32; ++j) {
-        float a, b;
-        if (kFoldScale) {
-          a = ex2(fmaf(x[2 * j], c, -base));
-          b = ex2(fmaf(x[2 * j + 1], c, -base));
-        } else {
-          a = ex2(x[2 * j] - base);
-          b = ex2(x[2 * j + 1] - base);
+            for (int j = 0; j < 4; ++j)
+              dst[j] = make_uint4(w[4 * j], w[4 * j + 1], w[4 * j + 2], w[4 * j + 3]);
+          }
         }
-        pk0[j] = pack_bf16x2(a, b);
-        lsum += bf16_lo(pk0[j]) + bf16_hi(pk0[j]);
-      }
-#pragma unroll
-      for (int j = 0; j < 32; ++j) {
-        float a, b;
-        if (kFoldScale) {
-          a = ex2(fmaf(x[64 + 2 * j], c, -base));
-          b = ex2(fmaf(x[64 + 2 * j + 1], c, -base));
-        } else {
-          a = ex2(x[64 + 2 * j] - base);
-          b = ex2(x[64 + 2 * j + 1] - base);
-        }
-        pk1[j] = pack_bf16x2(a, b);
-        lsum += bf16_lo(pk1[j]) + bf16_hi(pk1[j]);
-      }
-      l = l * alpha + lsum;
-
-      // O_X is stable here: the commit that signalled S_X(i) covers P_X(i-1) V.
-      if (__any_sync(0xffffffffu, rescale)) {
-        const float f = rescale ? alpha : 1.f;
+      } else {
+        // part of a pair: unnormalised fp32 partial, its exponent base and sum.
+        // Layout [column/4][row][4]: a warp's 32 rows store 512 contiguous bytes.
+        float* slot = p.ws + (size_t)it.slot * kSlotFloats;
+        const int R = X * kBM + row;
+        float4* ocol = reinterpret_cast<float4*>(slot) + R;
 #pragma unroll 1
         for (int c0 = 0; c0 < 128; c0 += 32) {
           uint32_t o[32];
           tmem_ld32(tO + c0, o);
           tmem_wait_ld(o);
 #pragma unroll
-          for (int j = 0; j < 32; ++j) o[j] = __float_as_uint(__uint_as_float(o[j]) * f);
-          tmem_st32(tO + c0, o);
+          for (int j = 0; j < 8; ++j)
+            ocol[(size_t)(c0 / 4 + j) * kPairRows] =
+                make_float4(__uint_as_float(o[4 * j]), __uint_as_float(o[4 * j + 1]),
+                            __uint_as_float(o[4 * j + 2]), __uint_as_float(o[4 * j + 3]));
         }
+        slot[(size_t)kPairRows * 128 + R] = m_run;
+        slot[(size_t)kPairRows * 128 + kPairRows + R] = l;
       }
-      tmem_st32(tS + 0, pk0);
-      tmem_st32(tS + 32, pk1);
-      tmem_wait_st();
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(bar(kBarP + X));
-    }
-
-    if (ok) {
-      ok = mbar_wait(bar(kBarO + X), 0, abort_flag, p.err, lim);
-      ok = __all_sync(0xffffffffu, ok);
-    }
-    if (ok) {
-      tc_fence_after();
-      const float inv = l > 0.f ? 1.f / l : 0.f;
-      __nv_bfloat16* orow = p.out + ((t * p.H + h) * (int64_t)128);
-#pragma unroll 1
-      for (int c0 = 0; c0 < 128; c0 += 32) {
-        uint32_t o[32];
-        tmem_ld32(tO + c0, o);
-        tmem_wait_ld(o);
-        uint32_t w[16];
-#pragma unroll
-        for (int j = 0; j < 16; ++j)
-          w[j] = pack_bf16x2(__uint_as_float(o[2 * j]) * inv, __uint_as_float(o[2 * j + 1]) * inv);
-        if (row_valid) {
-          uint4* dst = reinterpret_cast<uint4*>(orow + c0);
-#pragma unroll
-          for (int j = 0; j < 4; ++j)
-            dst[j] = make_uint4(w[4 * j], w[4 * j + 1], w[4 * j + 2], w[4 * j + 3]);
-        }
-      }
+      if (lane == 0) mbar_arrive(bar(kBarOFree + X));
     }
   }
 
@@ -433,33 +543,267 @@ bf16_d128_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
   }
 }
 
-}  // namespace
+// Combines the partial results of each split pair, in key order:
+// m = max_i m_i, O = sum_i 2^(m_i - m) O_i, l = sum_i 2^(m_i - m) l_i, out = O / l.
+// Block (e, g): merge entry e, columns 16 g .. 16 g + 15; thread R owns row R
+// (the partials' [column/4][row][4] layout makes every load coalesced across
+// the rows of a warp).  Up to kMergeUnroll pieces' loads are in flight at once.
+constexpr int kMergeCols = 16;
+constexpr int kMergeUnroll = 4;
 
-int launch_bf16_d128(const Call& c) {
-  static int attr_done[64] = {0};
-  if (c.device < 0 || c.device >= 64) return kErrDevice;
-  if (!attr_done[c.device]) {
-    if (cudaFuncSetAttribute(bf16_d128_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             kSmemAlloc) != cudaSuccess ||
-        cudaFuncSetAttribute(bf16_d128_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             kSmemAlloc) != cudaSuccess)
-      return kErrLaunch;
-    attr_done[c.device] = 1;
+__global__ void __launch_bounds__(kPairRows)
+merge_kernel(const Params p, const __grid_constant__ MergeSched ms) {
+  const MergeEntry e = ms.e[blockIdx.x];
+  const Unit u = unit_of(p, e.pair);
+  const int R = threadIdx.x;
+  const int X = R / kBM, row = R % kBM;
+  const int tok = row / p.group;
+  const int64_t t = (X ? u.t0B : u.t0A) + tok;
+  if (tok >= p.tok_per_tile || t >= p.T) return;
+  const int h = u.kh * p.group + row % p.group;
+  const int cq0 = blockIdx.y * (kMergeCols / 4);   // first column quad
+  const size_t off_m = (size_t)kPairRows * 128 + R, off_l = off_m + kPairRows;
+
+  float m = -INFINITY;
+  for (int i0 = 0; i0 < e.count; i0 += kMergeUnroll) {
+    float mi[kMergeUnroll];
+#pragma unroll
+    for (int j = 0; j < kMergeUnroll; ++j)
+      mi[j] = (i0 + j < e.count)
+                  ? p.ws[(size_t)ms.slots[e.first + i0 + j] * kSlotFloats + off_m]
+                  : -INFINITY;
+#pragma unroll
+    for (int j = 0; j < kMergeUnroll; ++j) m = fmaxf(m, mi[j]);
   }
-  const int group = c.H / c.Hkv;
-  const int tok_per_tile = kBM / group;  // group <= 128 checked by the caller
-  const int64_t tiles = (c.T + tok_per_tile - 1) / tok_per_tile;
+  const float mb = (m == -INFINITY) ? 0.f : m;
+  float4 acc[kMergeCols / 4];
+#pragma unroll
+  for (int q = 0; q < kMergeCols / 4; ++q) acc[q] = make_float4(0.f, 0.f, 0.f, 0.f);
+  float l = 0.f;
+  for (int i0 = 0; i0 < e.count; i0 += kMergeUnroll) {
+#pragma unroll
+    for (int j = 0; j < kMergeUnroll; ++j) {
+      if (i0 + j >= e.count) break;
+      const float* slot = p.ws + (size_t)ms.slots[e.first + i0 + j] * kSlotFloats;
+      const float w = ex2(slot[off_m] - mb);  // 0 for a piece that saw no visible key
+      l = fmaf(w, slot[off_l], l);
+      const float4* ocol = reinterpret_cast<const float4*>(slot) + R;
+#pragma unroll
+      for (int q = 0; q < kMergeCols / 4; ++q) {
+        const float4 o = ocol[(size_t)(cq0 + q) * kPairRows];
+        acc[q].x = fmaf(w, o.x, acc[q].x);
+        acc[q].y = fmaf(w, o.y, acc[q].y);
+        acc[q].z = fmaf(w, o.z, acc[q].z);
+        acc[q].w = fmaf(w, o.w, acc[q].w);
+      }
+    }
+  }
+  const float inv = l > 0.f ? 1.f / l : 0.f;
+  uint32_t wv[kMergeCols / 2];
+#pragma unroll
+  for (int q = 0; q < kMergeCols / 4; ++q) {
+    wv[2 * q] = pack_bf16x2(acc[q].x * inv, acc[q].y * inv);
+    wv[2 * q + 1] = pack_bf16x2(acc[q].z * inv, acc[q].w * inv);
+  }
+  uint4* dst = reinterpret_cast<uint4*>(p.out + (t * p.H + h) * (int64_t)128 + cq0 * 4);
+#pragma unroll
+  for (int q = 0; q < kMergeCols / 8; ++q)
+    dst[q] = make_uint4(wv[4 * q], wv[4 * q + 1], wv[4 * q + 2], wv[4 * q + 3]);
+}
+
+// ------------------------------------------------------------------ host
+struct Plan {
+  bool balanced = false;
+  int grid = 0;
+  size_t ws_bytes = 0;
+  Sched sched;
+  MergeSched merge;
+};
+
+struct Shape {
+  int64_t T, start_pos;
+  int H, Hkv, group, tok_per_tile, window, units_per_head, pairs;
+};
+
+bool make_shape(const Call& c, Shape* s) {
+  s->T = c.T;
+  s->start_pos = c.start_pos;
+  s->H = c.H;
+  s->Hkv = c.Hkv;
+  s->group = c.H / c.Hkv;
+  s->tok_per_tile = kBM / s->group;  // group <= 128 checked by the caller
+  s->window = c.window;
+  const int64_t tiles = (c.T + s->tok_per_tile - 1) / s->tok_per_tile;
   const int64_t units = (tiles + 1) / 2;
   const int64_t L = c.start_pos + c.T;
   if (units * c.Hkv > 0x7fffffff || L + kBN > 0x7fffffff ||
-      c.T + 2 * (int64_t)tok_per_tile > 0x7fffffff)
-    return kErrShape;
+      c.T + 2 * (int64_t)s->tok_per_tile > 0x7fffffff)
+    return false;
+  s->units_per_head = (int)units;
+  s->pairs = (int)(units * c.Hkv);
+  return true;
+}
 
+// Balanced schedule.  Each item costs its key tiles plus a fixed overhead
+// (reloading Q, refilling the pipeline, the epilogue), in key-tile units.
+// The pairs, in order, are cut into at most `ctas` consecutive runs of items
+// whose costs do not exceed a common budget; the smallest budget that covers
+// all pairs is found by bisection.  Returns false if the tables would
+// overflow (the caller then uses the plain schedule).
+constexpr int kItemOverheadTiles = 3;
+
+// Greedy cut for a given budget; returns the number of CTAs used (or
+// ctas + 1 if the budget is too small).  With `plan` it also fills the tables.
+int cut(const std::vector<int>& n, int64_t budget, int ctas, Plan* plan, int* n_items,
+        int* n_slots, std::vector<std::vector<int>>* pieces) {
+  const int pairs = (int)n.size();
+  int c = 0, items = 0, slots = 0;
+  int q = 0, done = 0;  // pair q, tiles of it already assigned
+  while (q < pairs) {
+    if (c >= ctas) return ctas + 1;
+    int64_t left = budget;
+    if (plan) plan->sched.cta_first[c] = items;
+    while (q < pairs && left > kItemOverheadTiles) {
+      const int rest = n[q] - done;
+      const int take = (int)std::min<int64_t>(rest, left - kItemOverheadTiles);
+      if (plan) {
+        if (items >= kMaxItems) return ctas + 1;
+        Item& it = plan->sched.items[items];
+        it.pair = q;
+        it.kb = done;
+        it.ke = done + take;
+        const bool whole = (done == 0 && take == n[q]);
+        it.slot = whole ? -1 : slots;
+        if (!whole) (*pieces)[q].push_back(slots);
+      }
+      ++items;
+      if (!(done == 0 && take == n[q])) ++slots;
+      left -= take + kItemOverheadTiles;
+      done += take;
+      if (done == n[q]) {
+        ++q;
+        done = 0;
+      }
+    }
+    ++c;
+  }
+  if (plan) plan->sched.cta_first[c] = items;
+  *n_items = items;
+  *n_slots = slots;
+  return c;
+}
+
+bool plan_balanced(const Shape& s, int ctas, Plan* plan) {
+  if (s.pairs <= 0) return false;
+  if (ctas > kMaxCtas) ctas = kMaxCtas;
+  std::vector<int> n(s.pairs);
+  int64_t W = 0;
+  int nmax = 0;
+  for (int pi = 0; pi < s.pairs; ++pi) {
+    n[pi] = unit_of(s.T, s.start_pos, s.Hkv, s.tok_per_tile, s.window, s.units_per_head, pi).n;
+    W += n[pi];
+    nmax = std::max(nmax, n[pi]);
+  }
+  // smallest budget (>= one tile plus overhead) that fits in `ctas` CTAs
+  int64_t lo = kItemOverheadTiles + 1, hi = W + (int64_t)s.pairs * kItemOverheadTiles + 1;
+  int items = 0, slots = 0;
+  while (lo < hi) {
+    const int64_t mid = (lo + hi) / 2;
+    if (cut(n, mid, ctas, nullptr, &items, &slots, nullptr) <= ctas)
+      hi = mid;
+    else
+      lo = mid + 1;
+  }
+  std::vector<std::vector<int>> pieces(s.pairs);
+  const int used = cut(n, lo, ctas, plan, &items, &slots, &pieces);
+  if (used > ctas || items > kMaxItems || slots > kMaxPieces) return false;
+  MergeSched& ms = plan->merge;
+  int ne = 0, np = 0;
+  for (int q = 0; q < s.pairs; ++q) {
+    if (pieces[q].empty()) continue;
+    if (ne >= kMaxMerge) return false;
+    MergeEntry& e = ms.e[ne++];
+    e.pair = q;
+    e.first = np;
+    e.count = (int)pieces[q].size();
+    e.pad = 0;
+    for (int sl : pieces[q]) ms.slots[np++] = sl;
+  }
+  ms.num = ne;
+  plan->sched.table = 1;
+  plan->balanced = true;
+  plan->grid = used;
+  plan->ws_bytes = (size_t)slots * kSlotBytes;
+  return true;
+}
+
+// The balanced schedule is used when the K/V stream is small enough to stay
+// in L2: its CTAs do not walk a kv head's keys in step, so without L2
+// residency they would each stream the keys from DRAM.  Larger caches use the
+// plain schedule, whose CTAs of one kv head advance through the keys together.
+constexpr int64_t kBalancedKvBytesMax = 96ll << 20;
+
+bool want_balanced(const Shape& s) {
+  const int64_t kv_bytes = 2ll * s.Hkv * (s.start_pos + s.T) * 128 * 2;
+  return kv_bytes <= kBalancedKvBytesMax;
+}
+
+}  // namespace
+
+size_t workspace_bytes_bf16_d128(const Call& c) {
+  Shape s;
+  if (!make_shape(c, &s) || !want_balanced(s)) return 0;
+  std::unique_ptr<Plan> plan(new Plan());
+  if (!plan_balanced(s, c.num_sms, plan.get())) return 0;
+  return plan->ws_bytes;
+}
+
+// One-time per-device set-up of both kernel variants: the shared-memory
+// opt-in, and a check that each was compiled with the register count the
+// warpgroup split assumes (a smaller pool would leave regs_increase waiting
+// forever, so such a kernel is never launched).
+int setup_kernel(const void* fn) {
+  if (cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemAlloc) !=
+      cudaSuccess)
+    return kErrLaunch;
+  cudaFuncAttributes a;
+  if (cudaFuncGetAttributes(&a, fn) != cudaSuccess) return kErrLaunch;
+  if ((int64_t)a.numRegs * kThreads < 8ll * 32 * kRegsSoftmax + 4ll * 32 * kRegsOther ||
+      a.maxThreadsPerBlock < kThreads)
+    return kErrLaunch;
+  return kOk;
+}
+
+int launch_bf16_d128(const Call& c) {
+  static int attr_state[64] = {0};  // 0: not checked, 1: ok, -1: unusable
+  if (c.device < 0 || c.device >= 64) return kErrDevice;
+  if (attr_state[c.device] == 0) {
+    const bool ok = setup_kernel((const void*)bf16_d128_kernel<true>) == kOk &&
+                    setup_kernel((const void*)bf16_d128_kernel<false>) == kOk;
+    attr_state[c.device] = ok ? 1 : -1;
+  }
+  if (attr_state[c.device] != 1) {
+    cudaGetLastError();
+    return kErrLaunch;
+  }
+  Shape s;
+  if (!make_shape(c, &s)) return kErrShape;
+
+  // The schedule tables are ~20 KB: built per call on the heap.
+  std::unique_ptr<Plan> plan(new Plan());
+  if (!(c.ws != nullptr && want_balanced(s) && plan_balanced(s, c.num_sms, plan.get()) &&
+        plan->ws_bytes <= c.ws_bytes)) {
+    plan->balanced = false;
+    plan->sched.table = 0;
+    plan->grid = s.pairs;
+  }
+
+  const int64_t L = c.start_pos + c.T;
   CUtensorMap tq, tk, tv;
   {
     const uint64_t dims[3] = {128, (uint64_t)c.H, (uint64_t)c.T};
     const uint64_t strides[2] = {128 * 2, (uint64_t)c.H * 128 * 2};
-    const uint32_t box[3] = {64, (uint32_t)group, (uint32_t)tok_per_tile};
+    const uint32_t box[3] = {64, (uint32_t)s.group, (uint32_t)s.tok_per_tile};
     if (encode_tmap_bf16_3d(&tq, c.q, dims, strides, box)) return kErrLaunch;
   }
   {
@@ -471,24 +815,32 @@ int launch_bf16_d128(const Call& c) {
   }
   Params p;
   p.out = static_cast<__nv_bfloat16*>(c.out);
+  p.ws = static_cast<float*>(c.ws);
   p.T = c.T;
   p.start_pos = c.start_pos;
   p.H = c.H;
   p.Hkv = c.Hkv;
-  p.group = group;
-  p.tok_per_tile = tok_per_tile;
+  p.group = s.group;
+  p.tok_per_tile = s.tok_per_tile;
   p.window = c.window;
-  p.units_per_head = (int)units;
+  p.units_per_head = s.units_per_head;
   p.scale_log2 = (float)((double)c.scale * 1.4426950408889634);
   p.err = c.err;
   p.wait_limit_ns = c.wait_limit_ns;
   p.flags = c.flags;
-  const dim3 grid((unsigned)(units * c.Hkv));
+  const dim3 grid((unsigned)plan->grid);
   if (p.scale_log2 > 0.f)
-    bf16_d128_kernel<true><<<grid, kThreads, kSmemAlloc, c.stream>>>(tq, tk, tv, p);
+    bf16_d128_kernel<true><<<grid, kThreads, kSmemAlloc, c.stream>>>(tq, tk, tv, p, plan->sched);
   else
-    bf16_d128_kernel<false><<<grid, kThreads, kSmemAlloc, c.stream>>>(tq, tk, tv, p);
-  return cudaGetLastError() == cudaSuccess ? kOk : kErrLaunch;
+    bf16_d128_kernel<false><<<grid, kThreads, kSmemAlloc, c.stream>>>(tq, tk, tv, p, plan->sched);
+  if (cudaGetLastError() != cudaSuccess) return kErrLaunch;
+  if (plan->balanced && plan->merge.num > 0) {
+    merge_kernel<<<dim3((unsigned)plan->merge.num, 128 / kMergeCols), kPairRows, 0,
+                   c.stream>>>(
+        p, plan->merge);
+    if (cudaGetLastError() != cudaSuccess) return kErrLaunch;
+  }
+  return kOk;
 }
 
 }  // namespace pfa

@@ -1,0 +1,431 @@
+// pfa_bf16_d512.cu -- fused flash-style prefill attention for bf16, head_dim 512
+// (the Gemma-style wide heads of the TensorSharp2 Gemma-4 prefill design,
+// section 2: the head_dim-512 flash kernel, and its sliding-window layers),
+// on the sm_103a tensor cores (tcgen05 + tensor memory + TMA).
+//
+// Operation: as for head_dim 128 (gnosis "Prefill attention -> GPU: handoff",
+// section "GPU design", steps 1-3, fused).
+//
+// Budget that shapes this kernel: a 128 x 512 fp32 output accumulator would
+// fill all 512 columns of tensor memory, leaving none for the scores, and one
+// 128 x 512 bf16 query tile takes 128 KB of the 227 KB of shared memory.  So a
+// CTA owns one 128-row query tile (group heads x 128/group tokens) of one kv
+// head and one half (256 columns) of the output head dimension.  The two CTAs
+// of a tile both compute the full S = Q K^T (contraction over all 512
+// dimensions) and each accumulates its half of P V: 1.5x the minimum tensor
+// work, in exchange for fitting S and O in tensor memory.
+//
+// Warp roles (7 warps):
+//   warps 0-3  softmax and epilogue (TMEM lanes 0-127, one row per thread)
+//   warp  4    TMA producer: Q once, then per key tile K (64 keys x 512) as
+//              eight 64-column chunks, each with its own slot and barriers
+//   warp  5    TMEM allocator and single-thread tcgen05.mma issuer
+//   warp  6    TMA producer: this CTA's half of V (64 keys x 256)
+// Q takes 128 KB of shared memory, so K and V have one tile slot each; K's
+// chunks are refilled one by one as the products reading them complete.
+//
+// Tensor memory: [0,64) S_0, [64,128) S_1 (double-buffered scores; after the
+// softmax the first 32 columns hold P as packed bf16 pairs), [256,512) O half.
+//
+// MMA issue order: S(0), S(1), O += P(0) V(0), S(2), O += P(1) V(1), ...
+// The softmax of tile i overlaps S(i+1); it waits for O += P(i-1) V(i-1)
+// (barrier kBarO, one phase per product) before it may rescale O.
+#include "pfa_internal.h"
+#include "pfa_ptx.cuh"
+
+#include <cuda_bf16.h>
+
+#include <cmath>
+
+namespace pfa {
+namespace {
+
+constexpr int kBM = 128;                  // query rows per tile
+constexpr int kBN = 64;                   // keys per K/V tile
+constexpr int kDHalf = 256;               // output columns per CTA
+constexpr int kQChunk = 128 * 128;        // 128 rows x 64 bf16 (one 128-byte swizzle span)
+constexpr int kKChunk = kBN * 128;        // 64 keys x 64 bf16
+constexpr int kSmemQ = 0;                 // 8 chunks: 128 KB
+constexpr int kSmemK = 8 * kQChunk;       // 8 chunks: 64 KB
+constexpr int kSmemV = kSmemK + 8 * kKChunk;   // 4 chunks: 32 KB
+constexpr int kSmemBars = kSmemV + 4 * kKChunk;  // 229376
+constexpr int kSmemAlloc = kSmemBars + 256 + 1024;
+constexpr int kThreads = 224;
+constexpr float kRescaleThreshold = 8.0f;
+
+constexpr int kBarQ = 0, kBarVFull = 1, kBarVEmpty = 2;
+constexpr int kBarS = 3;        // 2
+constexpr int kBarP = 5;        // 2
+constexpr int kBarO = 7;        // one phase per P V product
+constexpr int kBarDrain = 8;
+constexpr int kBarKFull = 9;    // 8: one per 64-column chunk of the K tile
+constexpr int kBarKEmpty = 17;  // 8
+constexpr int kNumBars = 25;
+static_assert(kNumBars * 8 + 8 <= 256, "barrier area");
+constexpr int kOffTmemSlot = kNumBars * 8;
+constexpr int kOffAbort = kOffTmemSlot + 4;
+
+constexpr uint32_t kColS = 0, kColO = 256;
+constexpr uint32_t kIdescQK = idesc_bf16_f32(kBM, kBN, false);
+constexpr uint32_t kIdescPV = idesc_bf16_f32(kBM, kDHalf, true);
+
+struct Params {
+  __nv_bfloat16* out;
+  int64_t T, start_pos;
+  int H, Hkv, group, tok_per_tile, window, tiles_per_head;
+  float scale_log2;
+  unsigned* err;
+  uint64_t wait_limit_ns;
+  int flags;
+};
+
+template <bool kFoldScale>
+__global__ void __launch_bounds__(kThreads, 1)
+bf16_d512_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+                 const __grid_constant__ CUtensorMap tm_v, const Params p) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  const uint32_t sbase = smem_u32(smem);
+  const uint32_t bars = sbase + kSmemBars;
+  auto bar = [&](int i) -> uint32_t { return bars + 8u * (uint32_t)i; };
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + kSmemBars + kOffTmemSlot);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + kSmemBars + kOffAbort);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const uint64_t lim = p.wait_limit_ns;
+
+  // work unit: (d-half, kv head, query tile); latest tokens first
+  const int dh = blockIdx.x & 1;
+  const int rest = blockIdx.x >> 1;
+  const int kh = rest % p.Hkv;
+  const int tile = p.tiles_per_head - 1 - rest / p.Hkv;
+  const int64_t t0 = (int64_t)tile * p.tok_per_tile;
+  const int64_t t_end = min(t0 + p.tok_per_tile, p.T);
+  const int64_t pos_first = p.start_pos + t0;
+  const int64_t pos_last = p.start_pos + t0 + p.tok_per_tile - 1;
+  const int64_t kmin = p.window > 0 ? max((int64_t)0, pos_first - p.window + 1) : 0;
+  const int64_t kt_first = kmin / kBN;
+  const int n = (int)((p.start_pos + t_end - 1) / kBN - kt_first + 1);
+
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < kNumBars; ++i)
+      mbar_init(bar(i), (i == kBarP || i == kBarP + 1) ? 4u : 1u);  // P: one arrival per softmax warp
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == 5) {
+    tmem_alloc(smem_u32(tmem_slot), 512);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  if (warp == 4 || warp == 6) {
+    // ------------------------------------------------------------ producers
+    // warp 4 loads Q once and then K tiles; warp 6 loads this CTA's V halves.
+    // Separate threads keep a K load from queueing behind the V buffer.
+    if (lane == 0) {
+      const bool is_k = (warp == 4);
+      const CUtensorMap* map = is_k ? &tm_k : &tm_v;
+      tma_prefetch_desc(map);
+      if (is_k) {
+        tma_prefetch_desc(&tm_q);
+        const int hq = kh * p.group;
+        mbar_arrive_expect_tx(bar(kBarQ), 8u * 128u * (uint32_t)(p.group * p.tok_per_tile));
+        for (int c = 0; c < 8; ++c)
+          tma_load_3d(sbase + kSmemQ + c * kQChunk, &tm_q, bar(kBarQ), 64 * c, hq, (int)t0);
+      }
+      if (is_k) {
+        // K: each 64-column chunk has its own slot and barriers, so chunk c of
+        // the next tile loads as soon as the products that read chunk c of
+        // this tile are done.
+        int issued = 0;  // tiles whose 8 chunks were all issued
+        int part = 0;    // chunks issued of the tile after those
+        bool ok = true;
+        for (int i = 0; i < n && ok; ++i) {
+          const int key0 = (int)((kt_first + i) * kBN);
+          for (int c = 0; c < 8; ++c) {
+            if (!(ok = mbar_wait(bar(kBarKEmpty + c), (uint32_t)(i & 1) ^ 1u, abort_flag, p.err,
+                                 lim)))
+              break;
+            mbar_arrive_expect_tx(bar(kBarKFull + c), (uint32_t)kKChunk);
+            tma_load_3d(sbase + kSmemK + c * kKChunk, map, bar(kBarKFull + c), 64 * c, key0, kh);
+            ++part;
+          }
+          if (ok) {
+            ++issued;
+            part = 0;
+          }
+        }
+        // no copy may be in flight when the CTA exits
+        mbar_wait(bar(kBarQ), 0, abort_flag, p.err, lim, true);
+        for (int c = 0; c < 8; ++c) {
+          const int loads = issued + (c < part ? 1 : 0);  // loads issued into chunk c
+          if (loads > 0)
+            mbar_wait(bar(kBarKFull + c), (uint32_t)(loads - 1) & 1u, abort_flag, p.err, lim, true);
+        }
+      } else {
+        int issued = 0;
+        for (int i = 0; i < n; ++i) {
+          const int key0 = (int)((kt_first + i) * kBN);
+          if (!mbar_wait(bar(kBarVEmpty), (uint32_t)(i & 1) ^ 1u, abort_flag, p.err, lim)) break;
+          mbar_arrive_expect_tx(bar(kBarVFull), (uint32_t)(4 * kKChunk));
+          for (int c = 0; c < 4; ++c)
+            tma_load_3d(sbase + kSmemV + c * kKChunk, map, bar(kBarVFull), dh * kDHalf + 64 * c,
+                        key0, kh);
+          ++issued;
+        }
+        if (issued > 0)
+          mbar_wait(bar(kBarVFull), (uint32_t)(issued - 1) & 1u, abort_flag, p.err, lim, true);
+      }
+    }
+  } else if (warp == 5) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      const uint32_t tO = tmem + kColO;
+      bool ok = mbar_wait(bar(kBarQ), 0, abort_flag, p.err, lim);
+      tc_fence_after();
+      bool issued = false;
+      auto pv = [&](int j) -> bool {  // O (+)= P(j) V(j)
+        if (!mbar_wait(bar(kBarP + (j & 1)), (uint32_t)(j >> 1) & 1u, abort_flag, p.err, lim))
+          return false;
+        if (!mbar_wait(bar(kBarVFull), (uint32_t)j & 1u, abort_flag, p.err, lim)) return false;
+        tc_fence_after();
+        const uint32_t tP = tmem + kColS + (uint32_t)((j & 1) * kBN);
+#pragma unroll
+        for (int kk = 0; kk < kBN / 16; ++kk)
+          mma_ts(tO, tP + kk * 8, sdesc_sw128(sbase + kSmemV + kk * 2048, kKChunk, 1024),
+                 kIdescPV, (j > 0 || kk > 0) ? 1u : 0u);
+        tc_commit(bar(kBarVEmpty));
+        tc_commit(bar(kBarO));
+        return true;
+      };
+      for (int i = 0; i < n && ok; ++i) {
+        const uint32_t tS = tmem + kColS + (uint32_t)((i & 1) * kBN);
+#pragma unroll 1
+        for (int c = 0; c < 8 && ok; ++c) {
+          if (!(ok = mbar_wait(bar(kBarKFull + c), (uint32_t)i & 1u, abort_flag, p.err, lim)))
+            break;
+          tc_fence_after();
+#pragma unroll
+          for (int kk = 0; kk < 4; ++kk) {
+            const uint32_t qa = sbase + kSmemQ + c * kQChunk + kk * 32;
+            const uint32_t ka = sbase + kSmemK + c * kKChunk + kk * 32;
+            mma_ss(tS, sdesc_sw128(qa, 16, 1024), sdesc_sw128(ka, 16, 1024), kIdescQK,
+                   (c > 0 || kk > 0) ? 1u : 0u);
+          }
+          issued = true;
+          tc_commit(bar(kBarKEmpty + c));
+        }
+        if (!ok) break;
+        tc_commit(bar(kBarS + (i & 1)));
+        if (i > 0 && !(ok = pv(i - 1))) break;
+      }
+      if (ok) ok = pv(n - 1);
+      if (issued) {
+        tc_commit(bar(kBarDrain));
+        mbar_wait(bar(kBarDrain), 0, abort_flag, p.err, lim, true);
+      }
+    }
+  } else {
+    // ------------------------------------------------------------ softmax
+    const int row = warp * 32 + lane;
+    const int tok = row / p.group;
+    const bool row_exists = tok < p.tok_per_tile;
+    const int64_t t = t0 + tok;
+    const bool row_valid = row_exists && t < p.T;
+    const int64_t pos = p.start_pos + t;
+    const int h = kh * p.group + row % p.group;
+    const uint32_t lane_off = (uint32_t)(warp * 32) << 16;
+    const uint32_t tO = tmem + lane_off + kColO;
+    const float c = p.scale_log2;
+
+    float m_run = -INFINITY, l = 0.f;
+    bool ok = true;
+    if (p.flags & kFlagForceTimeout) {
+      ok = mbar_wait(bar(kBarDrain), 0, abort_flag, p.err, lim);
+      ok = __all_sync(0xffffffffu, ok);
+    }
+    for (int i = 0; i < n && ok; ++i) {
+      ok = mbar_wait(bar(kBarS + (i & 1)), (uint32_t)(i >> 1) & 1u, abort_flag, p.err, lim);
+      if (!(ok = __all_sync(0xffffffffu, ok))) break;
+      tc_fence_after();
+      const uint32_t tS = tmem + lane_off + kColS + (uint32_t)((i & 1) * kBN);
+      uint32_t r0[32], r1[32];
+      tmem_ld32(tS, r0);
+      tmem_ld32(tS + 32, r1);
+      tmem_wait_ld(r0);
+      tmem_wait_ld(r1);
+      float x[64];
+#pragma unroll
+      for (int j = 0; j < 32; ++j) {
+        x[j] = __uint_as_float(r0[j]);
+        x[32 + j] = __uint_as_float(r1[j]);
+      }
+      if (!kFoldScale) {
+#pragma unroll
+        for (int j = 0; j < 64; ++j) x[j] *= c;
+      }
+      const int64_t key0 = (kt_first + i) * kBN;
+      const bool all_visible = (key0 + kBN - 1 <= pos_first) &&
+                               (p.window <= 0 || key0 > pos_last - p.window);
+      if (!all_visible) {
+        const int64_t hi = pos - key0;
+        const int64_t lo = p.window > 0 ? pos - p.window - key0 : -1;
+#pragma unroll
+        for (int j = 0; j < 64; ++j)
+          if (j > hi || j <= lo) x[j] = -INFINITY;
+      }
+      float pm[8];  // 8 independent partial max chains
+#pragma unroll
+      for (int a = 0; a < 8; ++a) pm[a] = x[a];
+#pragma unroll
+      for (int j = 8; j < 64; ++j) pm[j & 7] = fmaxf(pm[j & 7], x[j]);
+      float mx = fmaxf(fmaxf(fmaxf(pm[0], pm[1]), fmaxf(pm[2], pm[3])),
+                       fmaxf(fmaxf(pm[4], pm[5]), fmaxf(pm[6], pm[7])));
+      if (kFoldScale) mx *= c;
+      float alpha = 1.f;
+      bool rescale = false;
+      if (mx > m_run + kRescaleThreshold) {
+        alpha = ex2(m_run - mx);
+        rescale = (i > 0) && (m_run != -INFINITY);
+        m_run = mx;
+      }
+      const float base = (m_run == -INFINITY) ? 0.f : m_run;
+      uint32_t pk[32];
+      float ps[8];  // 8 independent partial row sums (of the bf16-rounded P)
+#pragma unroll
+      for (int a = 0; a < 8; ++a) ps[a] = 0.f;
+#pragma unroll
+      for (int j = 0; j < 32; ++j) {
+        float a, b;
+        if (kFoldScale) {
+          a = ex2(fmaf(x[2 * j], c, -base));
+          b = ex2(fmaf(x[2 * j + 1], c, -base));
+        } else {
+          a = ex2(x[2 * j] - base);
+          b = ex2(x[2 * j + 1] - base);
+        }
+        pk[j] = pack_bf16x2(a, b);
+        ps[j & 7] += bf16_lo(pk[j]) + bf16_hi(pk[j]);
+      }
+      const float lsum = ((ps[0] + ps[1]) + (ps[2] + ps[3])) + ((ps[4] + ps[5]) + (ps[6] + ps[7]));
+      l = l * alpha + lsum;
+      if (i > 0) {
+        // O (and the P buffer this tile reuses) are free once P(i-1) V is done.
+        ok = mbar_wait(bar(kBarO), (uint32_t)(i - 1) & 1u, abort_flag, p.err, lim);
+        if (!(ok = __all_sync(0xffffffffu, ok))) break;
+        tc_fence_after();
+      }
+      if (__any_sync(0xffffffffu, rescale)) {
+        const float f = rescale ? alpha : 1.f;
+#pragma unroll 1
+        for (int c0 = 0; c0 < kDHalf; c0 += 32) {
+          uint32_t o[32];
+          tmem_ld32(tO + c0, o);
+          tmem_wait_ld(o);
+#pragma unroll
+          for (int j = 0; j < 32; ++j) o[j] = __float_as_uint(__uint_as_float(o[j]) * f);
+          tmem_st32(tO + c0, o);
+        }
+      }
+      tmem_st32(tS, pk);
+      tmem_wait_st();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar(kBarP + (i & 1)));
+    }
+    if (ok) {
+      ok = mbar_wait(bar(kBarO), (uint32_t)(n - 1) & 1u, abort_flag, p.err, lim);
+      ok = __all_sync(0xffffffffu, ok);
+    }
+    if (ok) {
+      tc_fence_after();
+      const float inv = l > 0.f ? 1.f / l : 0.f;
+      __nv_bfloat16* orow = p.out + ((t * p.H + h) * (int64_t)512 + dh * kDHalf);
+#pragma unroll 1
+      for (int c0 = 0; c0 < kDHalf; c0 += 32) {
+        uint32_t o[32];
+        tmem_ld32(tO + c0, o);
+        tmem_wait_ld(o);
+        uint32_t w[16];
+#pragma unroll
+        for (int j = 0; j < 16; ++j)
+          w[j] = pack_bf16x2(__uint_as_float(o[2 * j]) * inv, __uint_as_float(o[2 * j + 1]) * inv);
+        if (row_valid) {
+          uint4* dst = reinterpret_cast<uint4*>(orow + c0);
+#pragma unroll
+          for (int j = 0; j < 4; ++j)
+            dst[j] = make_uint4(w[4 * j], w[4 * j + 1], w[4 * j + 2], w[4 * j + 3]);
+        }
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 5) {
+    tc_fence_after();
+    tmem_dealloc(tmem, 512);
+  }
+}
+
+}  // namespace
+
+int launch_bf16_d512(const Call& c) {
+  static int attr_done[64] = {0};
+  if (c.device < 0 || c.device >= 64) return kErrDevice;
+  if (!attr_done[c.device]) {
+    if (cudaFuncSetAttribute(bf16_d512_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             kSmemAlloc) != cudaSuccess ||
+        cudaFuncSetAttribute(bf16_d512_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             kSmemAlloc) != cudaSuccess)
+      return kErrLaunch;
+    attr_done[c.device] = 1;
+  }
+  const int group = c.H / c.Hkv;
+  const int tok_per_tile = kBM / group;
+  const int64_t tiles = (c.T + tok_per_tile - 1) / tok_per_tile;
+  const int64_t L = c.start_pos + c.T;
+  if (2 * tiles * c.Hkv > 0x7fffffff || L + kBN > 0x7fffffff) return kErrShape;
+
+  CUtensorMap tq, tk, tv;
+  {
+    const uint64_t dims[3] = {512, (uint64_t)c.H, (uint64_t)c.T};
+    const uint64_t strides[2] = {512 * 2, (uint64_t)c.H * 512 * 2};
+    const uint32_t box[3] = {64, (uint32_t)group, (uint32_t)tok_per_tile};
+    if (encode_tmap_bf16_3d(&tq, c.q, dims, strides, box)) return kErrLaunch;
+  }
+  {
+    const uint64_t dims[3] = {512, (uint64_t)L, (uint64_t)c.Hkv};
+    const uint64_t strides[2] = {512 * 2, (uint64_t)L * 512 * 2};
+    const uint32_t box[3] = {64, (uint32_t)kBN, 1};
+    if (encode_tmap_bf16_3d(&tk, c.k, dims, strides, box)) return kErrLaunch;
+    if (encode_tmap_bf16_3d(&tv, c.v, dims, strides, box)) return kErrLaunch;
+  }
+  Params p;
+  p.out = static_cast<__nv_bfloat16*>(c.out);
+  p.T = c.T;
+  p.start_pos = c.start_pos;
+  p.H = c.H;
+  p.Hkv = c.Hkv;
+  p.group = group;
+  p.tok_per_tile = tok_per_tile;
+  p.window = c.window;
+  p.tiles_per_head = (int)tiles;
+  p.scale_log2 = (float)((double)c.scale * 1.4426950408889634);
+  p.err = c.err;
+  p.wait_limit_ns = c.wait_limit_ns;
+  p.flags = c.flags;
+  const dim3 grid((unsigned)(2 * tiles * c.Hkv));
+  if (p.scale_log2 > 0.f)
+    bf16_d512_kernel<true><<<grid, kThreads, kSmemAlloc, c.stream>>>(tq, tk, tv, p);
+  else
+    bf16_d512_kernel<false><<<grid, kThreads, kSmemAlloc, c.stream>>>(tq, tk, tv, p);
+  return cudaGetLastError() == cudaSuccess ? kOk : kErrLaunch;
+}
+
+}  // namespace pfa

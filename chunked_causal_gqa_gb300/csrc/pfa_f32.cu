@@ -12,8 +12,9 @@
 // tiles of 32: lane j scores key j of the tile (a full dot product against the
 // warp's query row), the warp takes the tile maximum and sum with shuffles,
 // updates its online-softmax state and accumulates P.V with each lane owning
-// head_dim / 32 output columns.  The causal / window mask is evaluated from
-// the indices; no mask tensor exists.
+// head_dim / 32 output columns.  head_dim is a multiple of 4, so every row is
+// 16-byte aligned and moves as float4 vectors.  The causal / window mask is
+// evaluated from the indices; no mask tensor exists.
 #include "pfa_internal.h"
 #include "pfa_ptx.cuh"
 
@@ -26,6 +27,7 @@ constexpr int kRowsPerBlock = 8;      // one warp per row
 constexpr int kKeysPerTile = 32;
 constexpr int kMaxD = 512;
 constexpr int kMaxCols = kMaxD / 32;  // output columns per lane
+constexpr int kLoadBatch = 4;         // float4 loads in flight per thread and tensor
 
 struct F32Params {
   const float* q;
@@ -53,8 +55,10 @@ __global__ void __launch_bounds__(kRowsPerBlock * 32)
 f32_attention_kernel(const F32Params p) {
   extern __shared__ float smem[];
   const int D = p.D;
-  const int Dp = D + 1;                        // padded K rows: conflict-free column reads
-  float* sK = smem;                            // [32][D+1]
+  // K rows padded by 4 floats: lane j's 16-byte reads of row j fall in a
+  // distinct quarter of the banks for every 8 consecutive lanes.
+  const int Dp = D + 4;
+  float* sK = smem;                            // [32][D+4]
   float* sV = sK + kKeysPerTile * Dp;          // [32][D]
   float* sQ = sV + kKeysPerTile * D;           // [8][D]
 
@@ -88,25 +92,52 @@ f32_attention_kernel(const F32Params p) {
 
   for (int64_t j0 = kmin; j0 <= kmax; j0 += kKeysPerTile) {
     __syncthreads();  // previous tile fully consumed (and sQ written, first pass)
-    for (int idx = threadIdx.x; idx < kKeysPerTile * D; idx += blockDim.x) {
-      const int jj = idx / D, d = idx - jj * D;
-      const int64_t j = j0 + jj;
-      float kx = 0.f, vx = 0.f;
-      if (j <= kmax) {
-        kx = kbase[j * D + d];
-        vx = vbase[j * D + d];
+    // 4-float vectors; up to kLoadBatch vectors of K and of V per thread are
+    // loaded into registers before any is stored, so their DRAM latencies overlap.
+    const int nvec = kKeysPerTile * D / 4;
+    for (int base = threadIdx.x; base < nvec; base += kLoadBatch * blockDim.x) {
+      float4 kr4[kLoadBatch], vr4[kLoadBatch];
+#pragma unroll
+      for (int u = 0; u < kLoadBatch; ++u) {
+        const int idx = base + u * blockDim.x;
+        kr4[u] = make_float4(0.f, 0.f, 0.f, 0.f);
+        vr4[u] = kr4[u];
+        if (idx < nvec) {
+          const int jj = (idx * 4) / D;
+          const int64_t j = j0 + jj;
+          if (j <= kmax) {
+            const int d = idx * 4 - jj * D;
+            kr4[u] = *reinterpret_cast<const float4*>(kbase + j * D + d);
+            vr4[u] = *reinterpret_cast<const float4*>(vbase + j * D + d);
+          }
+        }
       }
-      sK[jj * Dp + d] = kx;
-      sV[jj * D + d] = vx;
+#pragma unroll
+      for (int u = 0; u < kLoadBatch; ++u) {
+        const int idx = base + u * blockDim.x;
+        if (idx < nvec) {
+          const int jj = (idx * 4) / D, d = idx * 4 - jj * D;
+          *reinterpret_cast<float4*>(sK + jj * Dp + d) = kr4[u];
+          *reinterpret_cast<float4*>(sV + jj * D + d) = vr4[u];
+        }
+      }
     }
     __syncthreads();
 
     // lane scores key j0 + lane
     const int64_t j = j0 + lane;
-    const float* qr = sQ + warp * D;
-    const float* kr = sK + lane * Dp;
-    float s = 0.f;
-    for (int d = 0; d < D; ++d) s = fmaf(qr[d], kr[d], s);
+    const float4* qr = reinterpret_cast<const float4*>(sQ + warp * D);
+    const float4* kr = reinterpret_cast<const float4*>(sK + lane * Dp);
+    float s0 = 0.f, s1 = 0.f, s2 = 0.f, s3 = 0.f;   // four independent chains
+#pragma unroll 4
+    for (int d4 = 0; d4 < D / 4; ++d4) {
+      const float4 a = qr[d4], b = kr[d4];
+      s0 = fmaf(a.x, b.x, s0);
+      s1 = fmaf(a.y, b.y, s1);
+      s2 = fmaf(a.z, b.z, s2);
+      s3 = fmaf(a.w, b.w, s3);
+    }
+    const float s = (s0 + s1) + (s2 + s3);
     const bool vis = active && j <= pos && (p.window <= 0 || j > pos - p.window);
     const float x = vis ? s * p.scale_log2 : -INFINITY;
 
@@ -141,7 +172,7 @@ f32_attention_kernel(const F32Params p) {
 }
 
 size_t smem_bytes(int D) {
-  return sizeof(float) * ((size_t)kKeysPerTile * (D + 1) + (size_t)kKeysPerTile * D +
+  return sizeof(float) * ((size_t)kKeysPerTile * (D + 4) + (size_t)kKeysPerTile * D +
                           (size_t)kRowsPerBlock * D);
 }
 

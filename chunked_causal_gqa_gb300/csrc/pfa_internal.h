@@ -22,6 +22,8 @@ struct Call {
   int flags;              // kFlag* bits
   int device;
   int num_sms;
+  void* ws;               // caller's workspace (device), may be null
+  size_t ws_bytes;
 };
 
 constexpr int kFlagForceTimeout = 1;
@@ -36,5 +38,8 @@ int encode_tmap_bf16_3d(CUtensorMap* out, const void* base, const uint64_t dims[
 
 int launch_f32(const Call& c);
 int launch_bf16_d128(const Call& c);
+// Workspace bytes the balanced head_dim-128 schedule needs (0: not used).
+size_t workspace_bytes_bf16_d128(const Call& c);
+int launch_bf16_d512(const Call& c);
 
 }  // namespace pfa

@@ -72,6 +72,14 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatil
   }
 }
 
+// mbar_wait executed by every lane of a converged warp; the result is the
+// same in all lanes (false if any lane gave up).
+__device__ __forceinline__ bool mbar_wait_warp(uint32_t bar, uint32_t parity,
+                                               volatile int* abort_flag, unsigned* err,
+                                               uint64_t limit_ns, bool ignore_abort = false) {
+  return __all_sync(0xffffffffu, mbar_wait(bar, parity, abort_flag, err, limit_ns, ignore_abort));
+}
+
 // ---------------------------------------------------------------- TMA
 __device__ __forceinline__ void tma_prefetch_desc(const CUtensorMap* map) {
   asm volatile("prefetch.tensormap [%0];" :: "l"(reinterpret_cast<uint64_t>(map)) : "memory");
@@ -147,6 +155,82 @@ __device__ __forceinline__ void mma_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_
                :: "r"(d_tmem), "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate) : "memory");
 }
 
+// ---- issue from a converged warp: every lane computes the (warp-uniform)
+// operands, one elected lane issues.  Keeping the issuing warp converged lets
+// the descriptors live in uniform registers; issuing from a lone lane of a
+// diverged warp makes every instruction pay for moving its operands.
+
+// Eight K=16 steps of D (+)= A * B with both operands in shared memory.
+// Step kk uses descriptors a0 + aoff(kk), b0 + boff(kk), where the offsets are
+// in 16-byte units (the descriptor's start-address field):
+//   kk = 0..3: + 2 kk,  kk = 4..7: + half + 2 (kk - 4)   (half = 64-column span)
+// The first step accumulates iff `accumulate`; the rest always accumulate.
+template <uint32_t kHalf16>
+__device__ __forceinline__ void mma8_ss_kmajor(uint32_t d_tmem, uint64_t a0, uint64_t b0,
+                                                uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred e, acc;\n\t.reg .b64 a, b;\n\t"
+      "elect.sync _|e, 0xffffffff;\n\t"
+      "setp.ne.b32 acc, %4, 0;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, acc;\n\t"
+      "add.s64 a, %1, 2;  add.s64 b, %2, 2;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], a, b, %3, e;\n\t"
+      "add.s64 a, %1, 4;  add.s64 b, %2, 4;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], a, b, %3, e;\n\t"
+      "add.s64 a, %1, 6;  add.s64 b, %2, 6;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], a, b, %3, e;\n\t"
+      "add.s64 a, %1, %5; add.s64 b, %2, %5;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], a, b, %3, e;\n\t"
+      "add.s64 a, %1, %6; add.s64 b, %2, %6;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], a, b, %3, e;\n\t"
+      "add.s64 a, %1, %7; add.s64 b, %2, %7;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], a, b, %3, e;\n\t"
+      "add.s64 a, %1, %8; add.s64 b, %2, %8;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], a, b, %3, e;\n\t}"
+      :: "r"(d_tmem), "l"(a0), "l"(b0), "r"(idesc), "r"(accumulate),
+         "n"(kHalf16), "n"(kHalf16 + 2), "n"(kHalf16 + 4), "n"(kHalf16 + 6)
+      : "memory");
+}
+
+// Eight K=16 steps of D (+)= A * B with A in tensor memory (columns a_tmem +
+// 8 kk, packed bf16 pairs) and B in shared memory (descriptor b0 + kk * bstep16,
+// offsets in 16-byte units).
+template <uint32_t kBStep16>
+__device__ __forceinline__ void mma8_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b0,
+                                        uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred e, acc;\n\t.reg .b64 b;\n\t.reg .b32 a;\n\t"
+      "elect.sync _|e, 0xffffffff;\n\t"
+      "setp.ne.b32 acc, %4, 0;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, acc;\n\t"
+      "add.s32 a, %1, 8;  add.s64 b, %2, %5;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [a], b, %3, e;\n\t"
+      "add.s32 a, %1, 16; add.s64 b, %2, %6;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [a], b, %3, e;\n\t"
+      "add.s32 a, %1, 24; add.s64 b, %2, %7;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [a], b, %3, e;\n\t"
+      "add.s32 a, %1, 32; add.s64 b, %2, %8;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [a], b, %3, e;\n\t"
+      "add.s32 a, %1, 40; add.s64 b, %2, %9;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [a], b, %3, e;\n\t"
+      "add.s32 a, %1, 48; add.s64 b, %2, %10;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [a], b, %3, e;\n\t"
+      "add.s32 a, %1, 56; add.s64 b, %2, %11;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [a], b, %3, e;\n\t}"
+      :: "r"(d_tmem), "r"(a_tmem), "l"(b0), "r"(idesc), "r"(accumulate),
+         "n"(kBStep16), "n"(2 * kBStep16), "n"(3 * kBStep16), "n"(4 * kBStep16),
+         "n"(5 * kBStep16), "n"(6 * kBStep16), "n"(7 * kBStep16)
+      : "memory");
+}
+
+// tcgen05.commit from one elected lane of a converged warp.
+__device__ __forceinline__ void tc_commit_elect(uint32_t bar) {
+  asm volatile(
+      "{\n\t.reg .pred e;\n\telect.sync _|e, 0xffffffff;\n\t"
+      "@e tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];\n\t}"
+      :: "r"(bar) : "memory");
+}
+
 // 32 consecutive 32-bit TMEM columns of this thread's lane -> r[0..31].
 __device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
   asm volatile("tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
@@ -163,6 +247,20 @@ __device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&r)[32
 }
 __device__ __forceinline__ void tmem_wait_st() {
   asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+}
+
+// ---------------------------------------------------------------- registers
+// Warpgroup-wide change of the per-thread register budget.  An increase
+// waits until other warpgroups of the CTA have released enough registers, so
+// the launcher must check that the CTA's pool (threads x registers at launch)
+// covers every warpgroup's share.
+template <int kRegs>
+__device__ __forceinline__ void regs_increase() {
+  asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" :: "n"(kRegs));
+}
+template <int kRegs>
+__device__ __forceinline__ void regs_decrease() {
+  asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" :: "n"(kRegs));
 }
 
 // ---------------------------------------------------------------- math

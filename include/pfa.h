@@ -93,7 +93,9 @@ typedef enum {
  * Ownership: the caller owns all four buffers and keeps them alive until the
  * work on `stream` completes.  The library allocates no device memory for
  * this call; it caches TMA tensor-map descriptors (host memory) keyed by
- * pointer and shape, and per-device launch attributes.
+ * pointer and shape, and per-device launch attributes.  It launches one
+ * kernel per call (one query-tile pair per CTA); see pfa_prefill_attention_ws
+ * for the balanced schedule.
  *
  * Behaviour: validates the arguments, then enqueues the kernel(s) on `stream`
  * and returns without synchronising.  Validation failures return a status
@@ -107,6 +109,45 @@ typedef enum {
 PFA_API int pfa_prefill_attention(const void *q, const void *k_cache, const void *v_cache, void *out,
                           int64_t T, int64_t start_pos, int num_heads, int num_kv_heads,
                           int head_dim, int window, float scale, int dtype, void *stream);
+
+/*
+ * pfa_prefill_attention_ws -- pfa_prefill_attention with a caller-provided
+ * device workspace that enables the balanced schedule.
+ *
+ *   workspace        device pointer (256-byte aligned) or NULL, not
+ *                    overlapping q, k_cache, v_cache or out.  Its contents on
+ *                    entry do not matter; the call may overwrite all of it.
+ *   workspace_bytes  its size.  If it is smaller than the value
+ *                    pfa_workspace_bytes reports for the same shape (or the
+ *                    workspace is NULL), the call uses the plain schedule,
+ *                    exactly as pfa_prefill_attention does.
+ *
+ * The balanced schedule (head_dim 128, bf16, caches small enough to stay in
+ * L2) cuts the key-tile work of all query tiles into one equal share per SM
+ * instead of one CTA per query-tile pair; query tiles whose keys are split
+ * between SMs leave fp32 partial results (output, exponent base, row sum) in
+ * the workspace, which a second kernel on the same stream combines in a fixed
+ * order.  The result is deterministic for a given device and shape, and equal
+ * to the plain schedule's within floating-point reassociation (both are
+ * within the stated tolerance of the exact result).  Concurrent calls must
+ * not share a workspace.  Other arguments, ownership and errors: as for
+ * pfa_prefill_attention (PFA_ERR_ALIGNMENT / PFA_ERR_DEVICE / PFA_ERR_ALIAS
+ * also cover the workspace).
+ */
+PFA_API int pfa_prefill_attention_ws(const void *q, const void *k_cache, const void *v_cache,
+                                     void *out, int64_t T, int64_t start_pos, int num_heads,
+                                     int num_kv_heads, int head_dim, int window, float scale,
+                                     int dtype, void *workspace, size_t workspace_bytes,
+                                     void *stream);
+
+/*
+ * pfa_workspace_bytes -- bytes of workspace the balanced schedule needs for
+ * this shape on the current device (0 when it would not be used).  Same
+ * shape validation as pfa_prefill_attention; no pointers are needed and
+ * nothing is launched.  Returns PFA_OK and sets *bytes, or an error status.
+ */
+PFA_API int pfa_workspace_bytes(int64_t T, int64_t start_pos, int num_heads, int num_kv_heads,
+                                int head_dim, int window, int dtype, size_t *bytes);
 
 /* Human-readable name of a pfa_status value (static storage, never NULL). */
 PFA_API const char *pfa_status_string(int status);

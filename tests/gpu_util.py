@@ -19,9 +19,10 @@ def dev():
     return torch.device("cuda", 0)
 
 
-def run(q, k, v, window=0, scale=None, out=None):
+def run(q, k, v, window=0, scale=None, out=None, workspace="auto"):
     d = dev()
-    o = pkg.prefill_attention(q.to(d), k.to(d), v.to(d), window=window, scale=scale, out=out)
+    o = pkg.prefill_attention(q.to(d), k.to(d), v.to(d), window=window, scale=scale, out=out,
+                              workspace=workspace)
     status = pkg.last_device_error()
     assert status == 0, f"device error status {status}"
     return o

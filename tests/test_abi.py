@@ -71,6 +71,18 @@ def test_argument_validation_without_gpu(lib):
     assert call(lib, o=B + 4096) == -9                 # out overlaps k_cache
 
 
+def test_workspace_entry_points_validate_without_gpu(lib):
+    n = ctypes.c_size_t(123)
+    assert lib.pfa_workspace_bytes(16, 0, 6, 4, 128, 0, BF16, ctypes.byref(n)) == -2
+    assert n.value == 0
+    assert lib.pfa_workspace_bytes(16, 0, 8, 2, 128, 0, BF16, None) == -1
+    assert lib.pfa_workspace_bytes(0, 0, 8, 2, 128, 0, BF16, ctypes.byref(n)) == 0
+    assert lib.pfa_prefill_attention_ws(A, B, C, O, 16, 0, 8, 2, 128, 0, 0.1, BF16,
+                                        0x70000000, 4096, None) in (-5,)   # no GPU here
+    assert lib.pfa_prefill_attention_ws(A, B, C, O, 16, 0, 6, 4, 128, 0, 0.1, BF16,
+                                        0x70000000, 4096, None) == -2
+
+
 def test_valid_arguments_reach_the_device_check(lib):
     import torch
     if torch.cuda.is_available():

@@ -33,6 +33,14 @@ BF16_CASES = [
     (8, 2, 128, 200, 0, 1000),     # window longer than the prompt
     (8, 2, 128, 1, 0, 0),          # a single first token
     (8, 2, 128, 1, 777, 0),        # a single token deep in the cache
+    # head_dim 512 (key tiles of 64, each CTA owning half of the output columns)
+    (8, 2, 512, 200, 100, 0),
+    (8, 2, 512, 130, 0, 64),       # window of exactly one key tile
+    (8, 2, 512, 150, 300, 1000),   # window longer than the visible prefix
+    (4, 4, 512, 150, 10, 0),       # group 1
+    (8, 1, 512, 40, 300, 100),     # group 8
+    (6, 2, 512, 70, 5, 0),         # group 3
+    (8, 2, 512, 1, 50, 0),
 ]
 
 
@@ -91,6 +99,31 @@ def test_long_chunk_sampled_parity(name):
     assert torch.isfinite(out.float()).all()
 
 
+def test_gemma_window_layer_full_parity():
+    wl = W.WORKLOADS["gemma_d512_window"]
+    q, k, v = W.make_inputs(wl)
+    got = G.to_np(G.run(q, k, v, window=wl.window, scale=wl.scale))
+    want = oracle.prefill_attention(q, k, v, window=wl.window, scale=wl.scale)
+    G.check(got, want, "bf16", wl.name)
+
+
+def test_gemma_global_layer_sampled_parity():
+    wl = W.WORKLOADS["gemma_d512_global"]
+    q, k, v = W.make_inputs(wl)
+    out = G.run(q, k, v, window=wl.window, scale=wl.scale)
+    rows = G.sample_rows(wl.T, wl.num_heads, 40, seed=wl.seeds[0])
+    want = oracle.prefill_attention_rows(q, k, v, rows, window=wl.window, scale=wl.scale)
+    got = G.to_np(out)[[t for t, _ in rows], [h for _, h in rows]]
+    G.check(got, want, "bf16", wl.name)
+
+
+@pytest.mark.parametrize("D", [128, 512])
+def test_repeated_runs_are_bit_identical_small(D):
+    q, k, v = (x.to(G.dev()) for x in W.make_random(333, 129, 8, 2, D, "bf16", seed=47))
+    digests = {G.digest(G.run(q, k, v, window=100)) for _ in range(5)}
+    assert len(digests) == 1
+
+
 def test_repeated_runs_are_bit_identical():
     wl = W.WORKLOADS["mistral_1358"]
     q, k, v = (x.to(G.dev()) for x in W.make_inputs(wl))
@@ -101,12 +134,55 @@ def test_repeated_runs_are_bit_identical():
 @pytest.mark.parametrize("window", [0, 200])
 def test_chunked_prefill_equals_one_shot(window):
     """Prefilling the second chunk against the cache gives the same rows as a
-    single prefill of the whole prompt."""
+    single prefill of the whole prompt: bit for bit with the plain schedule
+    (each row sees the same key tiles in the same order), and within rounding
+    with the balanced one (whose split points depend on the shape)."""
     H, Hkv, D, T1, T2 = 32, 8, 128, 384, 300
     q, k, v = W.make_random(T1 + T2, 0, H, Hkv, D, "bf16", seed=41, kv_std=0.5)
-    full = G.run(q, k, v, window=window)
-    chunk = G.run(q[T1:].contiguous(), k, v, window=window)
+    full = G.run(q, k, v, window=window, workspace=None)
+    chunk = G.run(q[T1:].contiguous(), k, v, window=window, workspace=None)
     assert torch.equal(chunk, full[T1:])
+    full_b = G.run(q, k, v, window=window)
+    chunk_b = G.run(q[T1:].contiguous(), k, v, window=window)
+    want = oracle.prefill_attention(q[T1:], k, v, window=window)
+    G.check(G.to_np(chunk_b), want, "bf16", "balanced chunk")
+    assert torch.allclose(chunk_b.float(), full_b[T1:].float(), atol=2e-2, rtol=1e-2)
+
+
+SCHEDULE_CASES = [
+    (32, 8, 128, 1358, 0, 0),
+    (8, 2, 128, 700, 3000, 0),
+    (8, 2, 128, 900, 100, 333),
+    (4, 4, 128, 520, 7, 0),
+    (16, 2, 128, 64, 5000, 0),
+    (8, 2, 128, 40, 3000, 0),      # fewer pairs than SMs: every pair is split
+]
+
+
+@pytest.mark.parametrize("case", SCHEDULE_CASES, ids=lambda c: "H%d_Hkv%d_D%d_T%d_sp%d_w%d" % c)
+def test_plain_and_balanced_schedules_agree_with_oracle(case):
+    import chunked_causal_gqa_gb300 as pkg
+    H, Hkv, D, T, sp, w = case
+    q, k, v = W.make_random(T, sp, H, Hkv, D, "bf16", seed=sum(case) + 7, kv_std=0.5)
+    want = oracle.prefill_attention(q, k, v, window=w)
+    plain = G.run(q, k, v, window=w, workspace=None)
+    G.check(G.to_np(plain), want, "bf16", "plain " + str(case))
+    assert pkg.workspace_bytes(T, sp, H, Hkv, D, w) > 0     # the balanced path is taken
+    bal = G.run(q, k, v, window=w)
+    G.check(G.to_np(bal), want, "bf16", "balanced " + str(case))
+    # an explicit workspace gives the same bits; one byte short falls back to plain
+    need = pkg.workspace_bytes(T, sp, H, Hkv, D, w)
+    ws = torch.full((need,), 255, dtype=torch.uint8, device=G.dev())
+    assert torch.equal(G.run(q, k, v, window=w, workspace=ws), bal)
+    small = torch.empty(need - 1, dtype=torch.uint8, device=G.dev())
+    assert torch.equal(G.run(q, k, v, window=w, workspace=small), plain)
+
+
+def test_balanced_schedule_is_bit_identical_across_runs():
+    wl = W.WORKLOADS["mistral_1358"]
+    q, k, v = (x.to(G.dev()) for x in W.make_inputs(wl))
+    digests = {G.digest(G.run(q, k, v, scale=wl.scale)) for _ in range(5)}
+    assert len(digests) == 1
 
 
 @pytest.mark.parametrize("window", [0, 150])
@@ -141,10 +217,17 @@ def test_group_heads_with_equal_queries_agree():
     assert torch.equal(out[:, 0], out[:, 1])
     assert torch.equal(out[:, 0], out[:, 3])
     assert not torch.equal(out[:, 0], out[:, 4])
+    q, k, v = W.make_random(T, sp, H, Hkv, 512, "bf16", seed=48)
+    q[:, 2] = q[:, 1]
+    q[:, 5] = q[:, 1]
+    out = G.run(q, k, v)
+    assert torch.equal(out[:, 1], out[:, 2])
+    assert not torch.equal(out[:, 1], out[:, 5])
 
 
-def test_window_one_returns_own_value_row():
-    H, Hkv, D, T, sp = 8, 2, 128, 200, 90
+@pytest.mark.parametrize("D", [128, 512])
+def test_window_one_returns_own_value_row(D):
+    H, Hkv, T, sp = 8, 2, 200, 90
     q, k, v = W.make_random(T, sp, H, Hkv, D, "bf16", seed=45)
     out = G.run(q, k, v, window=1).cpu()
     want = torch.stack([v[h // 4, sp:sp + T] for h in range(H)], dim=1)
