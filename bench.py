@@ -243,6 +243,8 @@ def run_ours(args, wl):
     stream = torch.cuda.current_stream(dev)
     ws_bytes = pkg.workspace_bytes(wl.T, wl.start_pos, wl.num_heads, wl.num_kv_heads,
                                    wl.head_dim, wl.window, W.torch_dtype(wl.dtype))
+    if args.schedule == "plain":
+        ws_bytes = 0
     workspace = torch.empty(ws_bytes, dtype=torch.uint8, device=dev) if ws_bytes > 0 else None
 
     def step():
@@ -299,11 +301,13 @@ def run_ours(args, wl):
         d2h = outp.numel() * outp.element_size()
         n_e2e = max(3, min(args.steps, 50))
         for _ in range(2):
-            pkg.prefill_attention(qp, kp, vp, out=outp, window=wl.window, scale=wl.scale)
+            pkg.prefill_attention(qp, kp, vp, out=outp, window=wl.window, scale=wl.scale,
+                              workspace="auto" if args.schedule == "auto" else None)
         torch.cuda.synchronize(dev)
         t0 = time.perf_counter()
         for _ in range(n_e2e):
-            pkg.prefill_attention(qp, kp, vp, out=outp, window=wl.window, scale=wl.scale)
+            pkg.prefill_attention(qp, kp, vp, out=outp, window=wl.window, scale=wl.scale,
+                              workspace="auto" if args.schedule == "auto" else None)
         torch.cuda.synchronize(dev)
         e2e_s = (time.perf_counter() - t0) / n_e2e
         if world > 1:
@@ -369,6 +373,8 @@ def main(argv=None):
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default="mistral_1358")
+    ap.add_argument("--schedule", choices=["auto", "plain"], default="auto",
+                    help="auto: balanced schedule with a workspace where the shape uses one")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=15.0,

@@ -21,12 +21,15 @@
 // combines the pieces of each such pair in a fixed order (the log-sum-exp
 // identity of the softmax; the result is deterministic).
 //
-// Warp roles (12 warps, three warpgroups):
+// Warp roles (10 warps):
 //   warps 0-3  softmax for tile A (TMEM lanes 0-127, one row per thread)
 //   warps 4-7  softmax for tile B
 //   warp  8    TMA producer: Q tiles of each item, K/V tiles into a 5-slot ring
-//   warp  9    TMEM allocator and single-thread tcgen05.mma issuer
-//   warps 10-11 idle (complete the third warpgroup)
+//   warp  9    TMEM allocator and MMA issuer.  The whole warp runs the issue
+//              loop, so the operand descriptors stay warp-uniform, and one
+//              elected lane issues each group of eight tcgen05.mma.  (Issuing
+//              from a lone lane of a diverged warp costs ~90 cycles per MMA,
+//              more than the 64 cycles an M=128 N=128 K=16 product takes.)
 //
 // Tensor memory (512 columns x 128 lanes, fp32 cells):
 //   [  0,128) S_A = Q_A K^T ; after softmax its first 64 columns hold P_A as
@@ -52,10 +55,8 @@
 // row's band are never loaded; tiles fully inside every row's band skip the
 // per-element test.
 //
-// Registers: three warps share each of the SM's four register-file partitions,
-// so a thread starts with at most 168 registers.  The third warpgroup drops
-// to kRegsOther and the softmax warpgroups rise to kRegsSoftmax, which a row
-// of 128 fp32 scores plus its packed probabilities needs.
+// Registers: 10 warps put three warps on some of the SM's four register-file
+// partitions, which caps a thread at 168 registers.
 #include "pfa_internal.h"
 #include "pfa_ptx.cuh"
 
@@ -75,12 +76,7 @@ constexpr int kBN = 128;                        // keys per K/V tile
 constexpr int kHalfBytes = 128 * 128;           // 128 rows x 64 bf16 (one 128-byte swizzle span)
 constexpr int kTileBytes = 2 * kHalfBytes;      // 128 rows x 128 bf16
 constexpr int kSlots = 5;                       // K/V ring depth (tiles)
-constexpr int kThreads = 384;
-constexpr int kRegsLaunch = 168;   // per thread, as compiled for 384 threads
-constexpr int kRegsSoftmax = 208;  // warpgroups 0 and 1 after the split
-constexpr int kRegsOther = 80;     // warpgroup 2 after the split
-static_assert(8 * 32 * kRegsSoftmax + 4 * 32 * kRegsOther <= kThreads * kRegsLaunch,
-              "register split exceeds the CTA's pool");
+constexpr int kThreads = 320;
 constexpr float kRescaleThreshold = 8.0f;       // log2 units
 
 constexpr int kSmemQ = 0;                                   // Q_A, Q_B
@@ -172,27 +168,6 @@ __device__ __forceinline__ Unit unit_of(const Params& p, int pidx) {
   return unit_of(p.T, p.start_pos, p.Hkv, p.tok_per_tile, p.window, p.units_per_head, pidx);
 }
 
-// 8 MMAs (K = 16 each) of S = Q K^T over d = 0..127.
-__device__ __forceinline__ void issue_qk(uint32_t tS, uint32_t q_addr, uint32_t k_addr) {
-#pragma unroll
-  for (int kk = 0; kk < 8; ++kk) {
-    const uint32_t off = (kk >> 2) * kHalfBytes + (kk & 3) * 32;
-    mma_ss(tS, sdesc_sw128(q_addr + off, 16, 1024), sdesc_sw128(k_addr + off, 16, 1024),
-           kIdescQK, kk > 0 ? 1u : 0u);
-  }
-}
-// 8 MMAs (K = 16 keys each) of O (+)= P V, P read from tensor memory.
-__device__ __forceinline__ void issue_pv(uint32_t tO, uint32_t tP, uint32_t v_addr,
-                                         bool accumulate) {
-#pragma unroll
-  for (int kk = 0; kk < 8; ++kk) {
-    // 16 keys = two 8-row groups (SBO 1024 B); d = 0..127 spans the two
-    // 64-column halves of the tile (LBO = one half).
-    mma_ts(tO, tP + kk * 8, sdesc_sw128(v_addr + kk * 2048, kHalfBytes, 1024), kIdescPV,
-           (accumulate || kk > 0) ? 1u : 0u);
-  }
-}
-
 template <bool kFoldScale>
 __global__ void __launch_bounds__(kThreads, 1)
 bf16_d128_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
@@ -241,7 +216,6 @@ bf16_d128_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
   const uint32_t tmem = *tmem_slot;
 
   if (warp >= 8) {
-   regs_decrease<kRegsOther>();
    if (warp == 8) {
     // ------------------------------------------------------------ producer
     if (lane == 0) {
@@ -288,9 +262,12 @@ bf16_d128_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
     }
    } else if (warp == 9) {
     // ------------------------------------------------------------ MMA issuer
-    if (lane == 0) {
+    // The whole warp runs this loop (operands stay warp-uniform); one elected
+    // lane issues each group of MMAs and each commit.
+    {
       const uint32_t tSA = tmem + 0, tSB = tmem + 128, tOA = tmem + 256, tOB = tmem + 384;
-      const uint32_t qA = sbase + kSmemQ, qB = sbase + kSmemQ + kTileBytes;
+      const uint64_t qdA = sdesc_sw128(sbase + kSmemQ, 16, 1024);
+      const uint64_t qdB = sdesc_sw128(sbase + kSmemQ + kTileBytes, 16, 1024);
       uint32_t li = 0;  // ring index of the next K tile
       uint32_t gi = 0;  // key tiles done by this CTA (phase of the S and P barriers)
       uint32_t kk = 0;  // items done
@@ -299,67 +276,69 @@ bf16_d128_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
       // the first P V product of the next item overwrites it.
       auto wait_o_free = [&](int X, int local_tile) -> bool {
         if (local_tile != 0 || kk == 0) return true;
-        return mbar_wait(bar(kBarOFree + X), (kk - 1) & 1u, abort_flag, p.err, lim);
+        return mbar_wait_warp(bar(kBarOFree + X), (kk - 1) & 1u, abort_flag, p.err, lim);
       };
       for (int k = item_begin; k < item_end && ok; ++k) {
         const Item it = get_item(k);
         const int n = it.ke - it.kb;
-        if (!(ok = mbar_wait(bar(kBarQ), kk & 1u, abort_flag, p.err, lim))) break;
+        if (!(ok = mbar_wait_warp(bar(kBarQ), kk & 1u, abort_flag, p.err, lim))) break;
         tc_fence_after();
         for (int i = 0; i < n; ++i) {
           const uint32_t ks = li % kSlots;
-          if (!(ok = mbar_wait(bar(kBarFull + ks), (li / kSlots) & 1u, abort_flag, p.err, lim)))
+          if (!(ok = mbar_wait_warp(bar(kBarFull + ks), (li / kSlots) & 1u, abort_flag, p.err, lim)))
             break;
           tc_fence_after();
           const uint32_t k_addr = sbase + kSmemRing + ks * kTileBytes;
-          issue_qk(tSA, qA, k_addr);
+          mma8_ss_kmajor<kHalfBytes / 16>(tSA, qdA, sdesc_sw128(k_addr, 16, 1024), kIdescQK, 0);
           issued = true;
-          tc_commit(bar(kBarS + 0));
+          tc_commit_elect(bar(kBarS + 0));
           if (i > 0) {
-            if (!(ok = mbar_wait(bar(kBarP + 1), (gi - 1) & 1u, abort_flag, p.err, lim))) break;
+            if (!(ok = mbar_wait_warp(bar(kBarP + 1), (gi - 1) & 1u, abort_flag, p.err, lim))) break;
             if (!(ok = wait_o_free(1, i - 1))) break;
             tc_fence_after();
             const uint32_t vs = (li - 1) % kSlots;  // V_{i-1}
-            issue_pv(tOB, tSB, sbase + kSmemRing + vs * kTileBytes, i - 1 > 0);
-            tc_commit(bar(kBarEmpty + vs));
+            mma8_ts<2048 / 16>(tOB, tSB, sdesc_sw128(sbase + kSmemRing + vs * kTileBytes, kHalfBytes, 1024), kIdescPV,
+                 (i - 1 > 0) ? 1u : 0u);
+            tc_commit_elect(bar(kBarEmpty + vs));
           }
-          issue_qk(tSB, qB, k_addr);
-          tc_commit(bar(kBarS + 1));
-          tc_commit(bar(kBarEmpty + ks));
-          if (i == n - 1) tc_commit(bar(kBarQFree));
+          mma8_ss_kmajor<kHalfBytes / 16>(tSB, qdB, sdesc_sw128(k_addr, 16, 1024), kIdescQK, 0);
+          tc_commit_elect(bar(kBarS + 1));
+          tc_commit_elect(bar(kBarEmpty + ks));
+          if (i == n - 1) tc_commit_elect(bar(kBarQFree));
           const uint32_t vs = (li + 1) % kSlots;  // V_i
-          if (!(ok = mbar_wait(bar(kBarFull + vs), ((li + 1) / kSlots) & 1u, abort_flag, p.err,
+          if (!(ok = mbar_wait_warp(bar(kBarFull + vs), ((li + 1) / kSlots) & 1u, abort_flag, p.err,
                                lim)))
             break;
-          if (!(ok = mbar_wait(bar(kBarP + 0), gi & 1u, abort_flag, p.err, lim))) break;
+          if (!(ok = mbar_wait_warp(bar(kBarP + 0), gi & 1u, abort_flag, p.err, lim))) break;
           if (!(ok = wait_o_free(0, i))) break;
           tc_fence_after();
-          issue_pv(tOA, tSA, sbase + kSmemRing + vs * kTileBytes, i > 0);
+          mma8_ts<2048 / 16>(tOA, tSA, sdesc_sw128(sbase + kSmemRing + vs * kTileBytes, kHalfBytes, 1024), kIdescPV,
+                 (i > 0) ? 1u : 0u);
           li += 2;
           ++gi;
         }
         if (!ok) break;
         // last product of tile B
-        if (!(ok = mbar_wait(bar(kBarP + 1), (gi - 1) & 1u, abort_flag, p.err, lim))) break;
+        if (!(ok = mbar_wait_warp(bar(kBarP + 1), (gi - 1) & 1u, abort_flag, p.err, lim))) break;
         if (!(ok = wait_o_free(1, n - 1))) break;
         tc_fence_after();
         const uint32_t vs = (li - 1) % kSlots;
-        issue_pv(tOB, tSB, sbase + kSmemRing + vs * kTileBytes, n - 1 > 0);
-        tc_commit(bar(kBarEmpty + vs));
-        tc_commit(bar(kBarO + 0));
-        tc_commit(bar(kBarO + 1));
+        mma8_ts<2048 / 16>(tOB, tSB, sdesc_sw128(sbase + kSmemRing + vs * kTileBytes, kHalfBytes, 1024), kIdescPV,
+                 (n - 1 > 0) ? 1u : 0u);
+        tc_commit_elect(bar(kBarEmpty + vs));
+        tc_commit_elect(bar(kBarO + 0));
+        tc_commit_elect(bar(kBarO + 1));
         ++kk;
       }
       if (issued) {
         // Everything issued must complete before TMEM is freed (this matters
         // when another role gave up early and skipped its wait on kBarO).
-        tc_commit(bar(kBarDrain));
-        mbar_wait(bar(kBarDrain), 0, abort_flag, p.err, lim, true);
+        tc_commit_elect(bar(kBarDrain));
+        mbar_wait_warp(bar(kBarDrain), 0, abort_flag, p.err, lim, true);
       }
     }
    }
   } else {
-    regs_increase<kRegsSoftmax>();
     // ------------------------------------------------------------ softmax
     const int X = warp >> 2;        // 0: tile A, 1: tile B
     const int wq = warp & 3;        // lane quarter
@@ -758,18 +737,10 @@ size_t workspace_bytes_bf16_d128(const Call& c) {
   return plan->ws_bytes;
 }
 
-// One-time per-device set-up of both kernel variants: the shared-memory
-// opt-in, and a check that each was compiled with the register count the
-// warpgroup split assumes (a smaller pool would leave regs_increase waiting
-// forever, so such a kernel is never launched).
+// One-time per-device set-up of a kernel variant: the shared-memory opt-in.
 int setup_kernel(const void* fn) {
   if (cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemAlloc) !=
       cudaSuccess)
-    return kErrLaunch;
-  cudaFuncAttributes a;
-  if (cudaFuncGetAttributes(&a, fn) != cudaSuccess) return kErrLaunch;
-  if ((int64_t)a.numRegs * kThreads < 8ll * 32 * kRegsSoftmax + 4ll * 32 * kRegsOther ||
-      a.maxThreadsPerBlock < kThreads)
     return kErrLaunch;
   return kOk;
 }

@@ -19,7 +19,8 @@
 //   warps 0-3  softmax and epilogue (TMEM lanes 0-127, one row per thread)
 //   warp  4    TMA producer: Q once, then per key tile K (64 keys x 512) as
 //              eight 64-column chunks, each with its own slot and barriers
-//   warp  5    TMEM allocator and single-thread tcgen05.mma issuer
+//   warp  5    TMEM allocator and MMA issuer (the whole warp runs the loop;
+//              one elected lane issues each group of tcgen05.mma)
 //   warp  6    TMA producer: this CTA's half of V (64 keys x 256)
 // Q takes 128 KB of shared memory, so K and V have one tile slot each; K's
 // chunks are refilled one by one as the products reading them complete.
@@ -184,50 +185,49 @@ bf16_d512_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
     }
   } else if (warp == 5) {
     // ------------------------------------------------------------ MMA issuer
-    if (lane == 0) {
+    // The whole warp runs this loop (operands stay warp-uniform); one elected
+    // lane issues each group of MMAs and each commit.
+    {
       const uint32_t tO = tmem + kColO;
-      bool ok = mbar_wait(bar(kBarQ), 0, abort_flag, p.err, lim);
+      bool ok = mbar_wait_warp(bar(kBarQ), 0, abort_flag, p.err, lim);
       tc_fence_after();
       bool issued = false;
       auto pv = [&](int j) -> bool {  // O (+)= P(j) V(j)
-        if (!mbar_wait(bar(kBarP + (j & 1)), (uint32_t)(j >> 1) & 1u, abort_flag, p.err, lim))
+        if (!mbar_wait_warp(bar(kBarP + (j & 1)), (uint32_t)(j >> 1) & 1u, abort_flag, p.err, lim))
           return false;
-        if (!mbar_wait(bar(kBarVFull), (uint32_t)j & 1u, abort_flag, p.err, lim)) return false;
+        if (!mbar_wait_warp(bar(kBarVFull), (uint32_t)j & 1u, abort_flag, p.err, lim))
+          return false;
         tc_fence_after();
         const uint32_t tP = tmem + kColS + (uint32_t)((j & 1) * kBN);
-#pragma unroll
-        for (int kk = 0; kk < kBN / 16; ++kk)
-          mma_ts(tO, tP + kk * 8, sdesc_sw128(sbase + kSmemV + kk * 2048, kKChunk, 1024),
-                 kIdescPV, (j > 0 || kk > 0) ? 1u : 0u);
-        tc_commit(bar(kBarVEmpty));
-        tc_commit(bar(kBarO));
+        // 64 keys = 4 steps of 16 (2048 B apart); N = 256 spans the 4 chunks of
+        // this CTA's V half (LBO = one chunk).
+        mma4_ts<2048 / 16>(tO, tP, sdesc_sw128(sbase + kSmemV, kKChunk, 1024), kIdescPV,
+                           j > 0 ? 1u : 0u);
+        tc_commit_elect(bar(kBarVEmpty));
+        tc_commit_elect(bar(kBarO));
         return true;
       };
       for (int i = 0; i < n && ok; ++i) {
         const uint32_t tS = tmem + kColS + (uint32_t)((i & 1) * kBN);
 #pragma unroll 1
         for (int c = 0; c < 8 && ok; ++c) {
-          if (!(ok = mbar_wait(bar(kBarKFull + c), (uint32_t)i & 1u, abort_flag, p.err, lim)))
+          if (!(ok = mbar_wait_warp(bar(kBarKFull + c), (uint32_t)i & 1u, abort_flag, p.err, lim)))
             break;
           tc_fence_after();
-#pragma unroll
-          for (int kk = 0; kk < 4; ++kk) {
-            const uint32_t qa = sbase + kSmemQ + c * kQChunk + kk * 32;
-            const uint32_t ka = sbase + kSmemK + c * kKChunk + kk * 32;
-            mma_ss(tS, sdesc_sw128(qa, 16, 1024), sdesc_sw128(ka, 16, 1024), kIdescQK,
-                   (c > 0 || kk > 0) ? 1u : 0u);
-          }
+          mma4_ss_kmajor(tS, sdesc_sw128(sbase + kSmemQ + c * kQChunk, 16, 1024),
+                         sdesc_sw128(sbase + kSmemK + c * kKChunk, 16, 1024), kIdescQK,
+                         c > 0 ? 1u : 0u);
           issued = true;
-          tc_commit(bar(kBarKEmpty + c));
+          tc_commit_elect(bar(kBarKEmpty + c));
         }
         if (!ok) break;
-        tc_commit(bar(kBarS + (i & 1)));
+        tc_commit_elect(bar(kBarS + (i & 1)));
         if (i > 0 && !(ok = pv(i - 1))) break;
       }
       if (ok) ok = pv(n - 1);
       if (issued) {
-        tc_commit(bar(kBarDrain));
-        mbar_wait(bar(kBarDrain), 0, abort_flag, p.err, lim, true);
+        tc_commit_elect(bar(kBarDrain));
+        mbar_wait_warp(bar(kBarDrain), 0, abort_flag, p.err, lim, true);
       }
     }
   } else {

@@ -223,6 +223,46 @@ __device__ __forceinline__ void mma8_ts(uint32_t d_tmem, uint32_t a_tmem, uint64
       : "memory");
 }
 
+// Four K=16 steps of D (+)= A * B, both operands K-major in shared memory
+// within one 128-byte swizzle span (steps advance both descriptors by 32 B).
+__device__ __forceinline__ void mma4_ss_kmajor(uint32_t d_tmem, uint64_t a0, uint64_t b0,
+                                               uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred e, acc;\n\t.reg .b64 a, b;\n\t"
+      "elect.sync _|e, 0xffffffff;\n\t"
+      "setp.ne.b32 acc, %4, 0;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, acc;\n\t"
+      "add.s64 a, %1, 2;  add.s64 b, %2, 2;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], a, b, %3, e;\n\t"
+      "add.s64 a, %1, 4;  add.s64 b, %2, 4;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], a, b, %3, e;\n\t"
+      "add.s64 a, %1, 6;  add.s64 b, %2, 6;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], a, b, %3, e;\n\t}"
+      :: "r"(d_tmem), "l"(a0), "l"(b0), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
+// Four K=16 steps of D (+)= A * B with A in tensor memory (columns a_tmem +
+// 8 kk) and B in shared memory (descriptor b0 + kk * bstep16, 16-byte units).
+template <uint32_t kBStep16>
+__device__ __forceinline__ void mma4_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b0,
+                                        uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred e, acc;\n\t.reg .b64 b;\n\t.reg .b32 a;\n\t"
+      "elect.sync _|e, 0xffffffff;\n\t"
+      "setp.ne.b32 acc, %4, 0;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, acc;\n\t"
+      "add.s32 a, %1, 8;  add.s64 b, %2, %5;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [a], b, %3, e;\n\t"
+      "add.s32 a, %1, 16; add.s64 b, %2, %6;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [a], b, %3, e;\n\t"
+      "add.s32 a, %1, 24; add.s64 b, %2, %7;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [a], b, %3, e;\n\t}"
+      :: "r"(d_tmem), "r"(a_tmem), "l"(b0), "r"(idesc), "r"(accumulate),
+         "n"(kBStep16), "n"(2 * kBStep16), "n"(3 * kBStep16)
+      : "memory");
+}
+
 // tcgen05.commit from one elected lane of a converged warp.
 __device__ __forceinline__ void tc_commit_elect(uint32_t bar) {
   asm volatile(
@@ -247,20 +287,6 @@ __device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&r)[32
 }
 __device__ __forceinline__ void tmem_wait_st() {
   asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
-}
-
-// ---------------------------------------------------------------- registers
-// Warpgroup-wide change of the per-thread register budget.  An increase
-// waits until other warpgroups of the CTA have released enough registers, so
-// the launcher must check that the CTA's pool (threads x registers at launch)
-// covers every warpgroup's share.
-template <int kRegs>
-__device__ __forceinline__ void regs_increase() {
-  asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" :: "n"(kRegs));
-}
-template <int kRegs>
-__device__ __forceinline__ void regs_decrease() {
-  asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" :: "n"(kRegs));
 }
 
 // ---------------------------------------------------------------- math
