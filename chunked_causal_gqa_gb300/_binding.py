@@ -19,10 +19,11 @@ PFA_BF16 = 1
 STATUS = {
     0: "PFA_OK", -1: "PFA_ERR_NULL", -2: "PFA_ERR_SHAPE", -3: "PFA_ERR_DTYPE",
     -4: "PFA_ERR_ALIGNMENT", -5: "PFA_ERR_DEVICE", -6: "PFA_ERR_LAUNCH",
-    -7: "PFA_ERR_TIMEOUT", -8: "PFA_ERR_VALUE", -9: "PFA_ERR_ALIAS",
+    -7: "PFA_ERR_TIMEOUT", -8: "PFA_ERR_VALUE", -9: "PFA_ERR_ALIAS", -10: "PFA_ERR_SCRATCH",
 }
 EXPORTS = ("pfa_prefill_attention", "pfa_prefill_attention_ws", "pfa_workspace_bytes",
-           "pfa_status_string", "pfa_last_device_error", "pfa_version", "pfa_debug_configure")
+           "pfa_prefill_attention_noalloc", "pfa_status_string", "pfa_last_device_error",
+           "pfa_version", "pfa_debug_configure")
 
 _lock = threading.Lock()
 _lib = None
@@ -58,6 +59,9 @@ def load(path: str | None = None) -> ctypes.CDLL:
         lib.pfa_workspace_bytes.argtypes = [i64, i64, i32, i32, i32, i32, i32,
                                             ctypes.POINTER(sz)]
         lib.pfa_workspace_bytes.restype = i32
+        lib.pfa_prefill_attention_noalloc.argtypes = [vp, vp, vp, vp, i64, i64, i32, i32, i32,
+                                                      i32, ctypes.c_float, i32, vp]
+        lib.pfa_prefill_attention_noalloc.restype = i32
         lib.pfa_status_string.argtypes = [i32]
         lib.pfa_status_string.restype = ctypes.c_char_p
         lib.pfa_last_device_error.argtypes = [vp]

@@ -197,6 +197,8 @@ const char* pfa_status_string(int status) {
     case PFA_ERR_TIMEOUT: return "PFA_ERR_TIMEOUT: a device-side wait gave up";
     case PFA_ERR_VALUE: return "PFA_ERR_VALUE: scale is not finite";
     case PFA_ERR_ALIAS: return "PFA_ERR_ALIAS: out overlaps an input";
+    case PFA_ERR_SCRATCH:
+      return "PFA_ERR_SCRATCH: the shape needs more scratch than the allocation-free entry holds";
     default: return "PFA: unknown status";
   }
 }
@@ -208,7 +210,9 @@ int pfa_debug_configure(double wait_limit_ms, int force_timeout) {
   return PFA_OK;
 }
 
-namespace {
+}  // extern "C"
+
+namespace pfa {
 
 // Validation shared by every entry point.  On success fills *c (without the
 // workspace) and returns PFA_OK; T == 0 returns PFA_OK with c->T == 0.
@@ -295,7 +299,9 @@ int dispatch(const Call& c, int dtype) {
   return rc;
 }
 
-}  // namespace
+}  // namespace pfa
+
+extern "C" {
 
 int pfa_prefill_attention(const void* q, const void* k_cache, const void* v_cache, void* out,
                           int64_t T, int64_t start_pos, int num_heads, int num_kv_heads,

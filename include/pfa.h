@@ -60,7 +60,9 @@ typedef enum {
     PFA_ERR_TIMEOUT = -7,    /* a device-side wait gave up (reported after a sync
                                 by pfa_last_device_error)                           */
     PFA_ERR_VALUE = -8,      /* scale is not a finite number                        */
-    PFA_ERR_ALIAS = -9       /* out overlaps q, k_cache or v_cache                  */
+    PFA_ERR_ALIAS = -9,      /* out overlaps q, k_cache or v_cache                  */
+    PFA_ERR_SCRATCH = -10    /* the shape needs more scratch than
+                                pfa_prefill_attention_noalloc holds                 */
 } pfa_status;
 
 /*
@@ -148,6 +150,45 @@ PFA_API int pfa_prefill_attention_ws(const void *q, const void *k_cache, const v
  */
 PFA_API int pfa_workspace_bytes(int64_t T, int64_t start_pos, int num_heads, int num_kv_heads,
                                 int head_dim, int window, int dtype, size_t *bytes);
+
+/*
+ * pfa_prefill_attention_noalloc -- the call of pfa_prefill_attention_ws with
+ * the balanced schedule, for callers that cannot allocate device memory.
+ * (The source pages have no counterpart: this is an interface convenience.)
+ *
+ * Who needs it: a caller that must not or cannot call cudaMalloc around the
+ * call -- code being captured into a CUDA graph, code under an allocator that
+ * owns all device memory, a host integration with no device allocator -- and
+ * so cannot hand pfa_prefill_attention_ws a workspace.  This entry point uses
+ * scratch memory that belongs to the library instead: a static array of
+ * PFA_NOALLOC_SCRATCH_BYTES (32 MiB) in device memory, present on every
+ * device where the library's code has been loaded, until the process exits.
+ * It allocates nothing: no cudaMalloc/cudaFree and no allocating library
+ * routine is called.
+ *
+ * Arguments, layouts, ownership and the result: as for pfa_prefill_attention.
+ * For bf16 with head_dim 128 it runs the balanced schedule in the static
+ * scratch; a shape whose balanced schedule needs more than
+ * PFA_NOALLOC_SCRATCH_BYTES is refused with PFA_ERR_SCRATCH before anything
+ * is launched.  Shapes that use no workspace (other dtypes or head_dims, or
+ * caches too large for the balanced schedule) run as pfa_prefill_attention.
+ *
+ * Sharing: every call on a device uses the same scratch and leaves its own
+ * partial results in it.  No part of it needs to be zero on entry (a call
+ * only reads what it wrote itself).  Calls whose kernels may overlap on the
+ * GPU -- on different streams without an ordering between them -- race on
+ * the scratch and can return wrong results; order them.
+ *
+ * Set-up: the first call on a device looks up the scratch's device address
+ * (cudaGetSymbolAddress, with that device current).  Make that first call
+ * before any stream capture that includes this entry point.
+ */
+#define PFA_NOALLOC_SCRATCH_BYTES (32u << 20)
+PFA_API int pfa_prefill_attention_noalloc(const void *q, const void *k_cache,
+                                          const void *v_cache, void *out, int64_t T,
+                                          int64_t start_pos, int num_heads, int num_kv_heads,
+                                          int head_dim, int window, float scale, int dtype,
+                                          void *stream);
 
 /* Human-readable name of a pfa_status value (static storage, never NULL). */
 PFA_API const char *pfa_status_string(int status);
