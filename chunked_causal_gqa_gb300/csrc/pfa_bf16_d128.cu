@@ -19,7 +19,10 @@
 // overhead); an item that covers only part of a pair writes its unnormalised
 // partial (O, exponent base, row sum) to a workspace slot, and merge_kernel
 // combines the pieces of each such pair in a fixed order (the log-sum-exp
-// identity of the softmax; the result is deterministic).
+// identity of the softmax; the result is deterministic).  The host uses the
+// balanced schedule only where its estimated makespan clearly beats the plain
+// one's: chiefly short chunks deep into long contexts, where the plain
+// schedule has fewer pairs than SMs.
 //
 // Warp roles (10 warps):
 //   warps 0-3  softmax for tile A (TMEM lanes 0-127, one row per thread)
@@ -716,24 +719,61 @@ bool plan_balanced(const Shape& s, int ctas, Plan* plan) {
   return true;
 }
 
-// The balanced schedule is used when the K/V stream is small enough to stay
-// in L2: its CTAs do not walk a kv head's keys in step, so without L2
-// residency they would each stream the keys from DRAM.  Larger caches use the
-// plain schedule, whose CTAs of one kv head advance through the keys together.
+// Cost of the merge kernel and of writing and reading the partials, in
+// key-tile units (a measured few microseconds).
+constexpr int64_t kMergeCostTiles = 3;
+
+// Makespan of the plain schedule in key-tile units: the hardware starts CTAs
+// in pair order on the first SM that frees up, each costing its key tiles
+// plus the per-item overhead.
+int64_t plain_makespan(const Shape& s, int sms) {
+  std::vector<int64_t> free_at((size_t)std::max(sms, 1), 0);  // min-heap of SM finish times
+  int64_t makespan = 0;
+  for (int pi = 0; pi < s.pairs; ++pi) {
+    std::pop_heap(free_at.begin(), free_at.end(), std::greater<int64_t>());
+    const int n = unit_of(s.T, s.start_pos, s.Hkv, s.tok_per_tile, s.window, s.units_per_head,
+                          pi).n;
+    free_at.back() += n + kItemOverheadTiles;
+    makespan = std::max(makespan, free_at.back());
+    std::push_heap(free_at.begin(), free_at.end(), std::greater<int64_t>());
+  }
+  return makespan;
+}
+
+// Whether the balanced schedule may be used.  Its CTAs do not walk a kv
+// head's keys in step, so when many pairs of a large cache are in flight
+// each CTA would stream its keys from DRAM; it is allowed when the K/V cache
+// stays in L2, or when there are no more pairs than SMs (then each CTA reads
+// its own key range once).
 constexpr int64_t kBalancedKvBytesMax = 96ll << 20;
 
-bool want_balanced(const Shape& s) {
+bool balanced_allowed(const Shape& s, int sms) {
   const int64_t kv_bytes = 2ll * s.Hkv * (s.start_pos + s.T) * 128 * 2;
-  return kv_bytes <= kBalancedKvBytesMax;
+  return kv_bytes <= kBalancedKvBytesMax || s.pairs <= sms;
+}
+
+// Plans the balanced schedule and keeps it only if it is expected to beat the
+// plain one by a clear margin (15%).
+bool choose_balanced(const Shape& s, int sms, Plan* plan) {
+  if (!balanced_allowed(s, sms) || !plan_balanced(s, sms, plan)) return false;
+  if (plan->merge.num == 0) return false;  // nothing split: same as plain
+  int64_t budget = 0;
+  for (int c = 0; c < plan->grid; ++c) {
+    int64_t cost = 0;
+    for (int k = plan->sched.cta_first[c]; k < plan->sched.cta_first[c + 1]; ++k)
+      cost += plan->sched.items[k].ke - plan->sched.items[k].kb + kItemOverheadTiles;
+    budget = std::max(budget, cost);
+  }
+  return 100 * (budget + kMergeCostTiles) < 85 * plain_makespan(s, sms);
 }
 
 }  // namespace
 
 size_t workspace_bytes_bf16_d128(const Call& c) {
   Shape s;
-  if (!make_shape(c, &s) || !want_balanced(s)) return 0;
+  if (!make_shape(c, &s)) return 0;
   std::unique_ptr<Plan> plan(new Plan());
-  if (!plan_balanced(s, c.num_sms, plan.get())) return 0;
+  if (!choose_balanced(s, c.num_sms, plan.get())) return 0;
   return plan->ws_bytes;
 }
 
@@ -762,7 +802,7 @@ int launch_bf16_d128(const Call& c) {
 
   // The schedule tables are ~20 KB: built per call on the heap.
   std::unique_ptr<Plan> plan(new Plan());
-  if (!(c.ws != nullptr && want_balanced(s) && plan_balanced(s, c.num_sms, plan.get()) &&
+  if (!(c.ws != nullptr && choose_balanced(s, c.num_sms, plan.get()) &&
         plan->ws_bytes <= c.ws_bytes)) {
     plan->balanced = false;
     plan->sched.table = 0;

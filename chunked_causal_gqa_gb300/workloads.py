@@ -92,6 +92,10 @@ WORKLOADS = {
     "gemma_d512_global": Workload(
         "gemma_d512_global", 8, 2, 512, 2048, 6144, 0, "bf16", 1.0, 1.0, (4000, 4001, 4002),
         "head_dim-512 global causal layer, bf16: H=8, Hkv=2, T=2048 at start_pos=6144"),
+    "chunk_64k_t128": Workload(
+        "chunk_64k_t128", 32, 8, 128, 128, 63360, 0, "bf16", 1.0, 0.5, (3100, 3101, 3102),
+        "128-token chunk at start_pos=63360 (L=63488), bf16: H=32, Hkv=8, D=128 "
+        "(fewer query-tile pairs than SMs)"),
     "chunk_128k": Workload(
         "chunk_128k", 32, 8, 128, 2048, 129024, 0, "bf16", 1.0, 0.5, (5000, 5001, 5002),
         "2048-token chunk at start_pos=129024 (L=131072), bf16: H=32, Hkv=8, D=128"),

@@ -32,11 +32,12 @@ def _call_noalloc(lib, q, k, v, out, start_pos, window, scale):
         window, float(scale), PFA_BF16, torch.cuda.current_stream().cuda_stream)
 
 
+# Shapes that use the balanced schedule (short chunks deep into the cache).
 CASES = [
     # (H, Hkv, D, T, start_pos, window)
-    (32, 8, 128, 1358, 0, 0),      # the Mistral-shaped prompt layer
-    (8, 2, 128, 300, 200, 0),
-    (8, 2, 128, 900, 100, 333),    # sliding window
+    (32, 8, 128, 128, 30000, 0),
+    (8, 2, 128, 300, 20000, 0),
+    (8, 2, 128, 200, 8000, 2048),   # sliding window
 ]
 
 
@@ -62,15 +63,18 @@ def test_noalloc_matches_the_workspace_entry_on_two_calls_in_a_row(case):
 def test_noalloc_refuses_a_shape_beyond_its_scratch():
     lib = _binding.load()
     d = G.dev()
-    # shapes whose balanced schedule needs a little more than 32 MiB on a 152-SM GB300
-    candidates = [(32, 8, 1024, 5000), (32, 4, 1024, 5000), (64, 8, 512, 5000),
-                  (32, 4, 1024, 20000), (16, 8, 2048, 20000), (64, 8, 1024, 5000)]
+    # 1k-token chunks at start_pos 120000: their balanced schedule needs a
+    # little more than 32 MiB on a 152-SM GB300
+    candidates = [(32, 4, 1024, 120000), (32, 8, 1024, 120000), (64, 8, 512, 120000)]
     for H, Hkv, T, sp in candidates:
         if pkg.workspace_bytes(T, sp, H, Hkv, 128, 0) > SCRATCH_BYTES:
             break
     else:
         pytest.fail("no candidate shape needs more than the static scratch on this device")
-    q, k, v = (x.to(d) for x in W.make_random(T, sp, H, Hkv, 128, "bf16", seed=62))
+    L = sp + T
+    q = torch.empty(T, H, 128, dtype=torch.bfloat16, device=d)   # refused before any launch
+    k = torch.empty(Hkv, L, 128, dtype=torch.bfloat16, device=d)
+    v = torch.empty_like(k)
     out = torch.empty_like(q)
     assert _call_noalloc(lib, q, k, v, out, sp, 0, 128 ** -0.5) == -10     # PFA_ERR_SCRATCH
     assert lib.pfa_status_string(-10).decode().startswith("PFA_ERR_SCRATCH")
