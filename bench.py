@@ -7,7 +7,7 @@ default workload is the Mistral-7B-shaped layer (32 query heads, 8 kv heads,
 head_dim 128, a 1358-token prompt, bf16); --workload selects another.
 
 Timing: W untimed warm-up steps; then K steps, each preceded (outside its
-timed span) by a 256 MiB write that flushes L2, each timed with CUDA events on
+timed span) by a 512 MiB write that flushes L2, each timed with CUDA events on
 the launching stream; barrier + synchronize on both sides; max over ranks.
 Metric: causal attention TFLOP/s = 4 * head_dim * num_heads * (sum over query
 tokens of visible keys) / time, 2 flops per multiply-add.
@@ -22,6 +22,7 @@ independent), and rank 0 prints one JSON line.
 from __future__ import annotations
 
 import argparse
+import gc
 import hashlib
 import json
 import os
@@ -239,7 +240,10 @@ def run_ours(args, wl):
     q_h, k_h, v_h = W.make_inputs(wl)
     q, k, v = q_h.to(dev), k_h.to(dev), v_h.to(dev)
     out = torch.empty_like(q)
-    flush = torch.empty(256 * 1024 * 1024, dtype=torch.uint8, device=dev)
+    # L2 flush between timed steps: a 512 MiB write (4x L2).  It also keeps the
+    # GPU busy long enough for the next step's launches to be queued before
+    # its start event, so host-side launch latency never lands inside a span.
+    flush = torch.empty(512 * 1024 * 1024, dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream(dev)
     ws_bytes = pkg.workspace_bytes(wl.T, wl.start_pos, wl.num_heads, wl.num_kv_heads,
                                    wl.head_dim, wl.window, W.torch_dtype(wl.dtype))
@@ -267,6 +271,8 @@ def run_ours(args, wl):
     if world > 1:
         dist.barrier()
     torch.cuda.synchronize(dev)
+    gc_was_enabled = gc.isenabled()
+    gc.disable()
     wall0 = time.perf_counter()
     for e0, e1 in events:
         flush.fill_(1)
@@ -275,6 +281,8 @@ def run_ours(args, wl):
         e1.record(stream)
     torch.cuda.synchronize(dev)
     wall = time.perf_counter() - wall0
+    if gc_was_enabled:
+        gc.enable()
     if world > 1:
         dist.barrier()
     clocks = sampler.stop()
@@ -349,7 +357,7 @@ def run_ours(args, wl):
                        "num_heads": wl.num_heads, "num_kv_heads": wl.num_kv_heads,
                        "head_dim": wl.head_dim, "T": wl.T, "start_pos": wl.start_pos,
                        "window": wl.window, "seeds": list(wl.seeds),
-                       "l2": "flushed before every timed step (256 MiB write)",
+                       "l2": "flushed before every timed step (512 MiB write)",
                        "parallelism": f"replicas x{world}"},
             "prompt_tok_s_per_layer": world * wl.T / (ms_step * 1e-3),
             "frac_of_bf16_peak": value / world / float(peaks["bf16_tflops"]),

@@ -50,8 +50,8 @@
 // Online softmax in the log2 domain (scores pre-multiplied by scale*log2 e).
 // The running maximum used as the exponent base is only raised when a new
 // row maximum exceeds it by more than 2^8, so O is rescaled rarely; the final
-// normalisation O / l is exact for any base.  l is summed from the same
-// bf16-rounded P that feeds the P V product.
+// normalisation O / l is exact for any base.  l is summed from the fp32
+// probabilities before their rounding to bf16 for the P V product.
 //
 // Masks come from indices: key j is visible to a row at position pos iff
 // j <= pos and (window <= 0 or j > pos - window).  Key tiles outside every
@@ -410,11 +410,21 @@ bf16_d128_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
           for (int j = 0; j < 128; ++j)
             if (j > hi || j <= lo) x[j] = -INFINITY;
         }
-        //@@MAX_BEGIN
-        float mx = -INFINITY;
+        // Row max with three-input max instructions in 8 independent chains.
+        float mx;
+        {
+          float m[8];
 #pragma unroll
-        for (int j = 0; j < 128; ++j) mx = fmaxf(mx, x[j]);
-        //@@MAX_END
+          for (int q = 0; q < 8; ++q) m[q] = max3f(x[q], x[8 + q], x[16 + q]);
+#pragma unroll
+          for (int j = 24; j < 120; j += 16) {
+#pragma unroll
+            for (int q = 0; q < 8; ++q) m[q] = max3f(m[q], x[j + q], x[j + 8 + q]);
+          }
+#pragma unroll
+          for (int q = 0; q < 8; ++q) m[q] = fmaxf(m[q], x[120 + q]);
+          mx = max3f(max3f(m[0], m[1], m[2]), max3f(m[3], m[4], m[5]), fmaxf(m[6], m[7]));
+        }
         if (kFoldScale) mx *= c;
 
         // Raise the exponent base only when the new maximum exceeds it by > 2^8.
@@ -427,10 +437,12 @@ bf16_d128_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
         }
         const float base = (m_run == -INFINITY) ? 0.f : m_run;
 
-        // P = 2^(s - base) as packed bf16 pairs; l gains the sum of the rounded values.
+        // P = 2^(s - base) as packed bf16 pairs; l gains the row sum of the
+        // unrounded values (8 independent partial sums).
         uint32_t pk0[32], pk1[32];
-        //@@EXP_BEGIN
-        float lsum = 0.f;
+        float ls[8];
+#pragma unroll
+        for (int q = 0; q < 8; ++q) ls[q] = 0.f;
 #pragma unroll
         for (int j = 0; j < 64; ++j) {
           const float xa = x[2 * j], xb = x[2 * j + 1];
@@ -438,9 +450,10 @@ bf16_d128_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
           const float pb = kFoldScale ? ex2(fmaf(xb, c, -base)) : ex2(xb - base);
           const uint32_t w = pack_bf16x2(pa, pb);
           if (j < 32) pk0[j] = w; else pk1[j - 32] = w;
-          lsum += bf16_lo(w) + bf16_hi(w);
+          ls[(2 * j) & 7] += pa;
+          ls[(2 * j + 1) & 7] += pb;
         }
-        //@@EXP_END
+        const float lsum = ((ls[0] + ls[1]) + (ls[2] + ls[3])) + ((ls[4] + ls[5]) + (ls[6] + ls[7]));
         l = l * alpha + lsum;
 
         // O_X is stable here: the commit that signalled S_X(i) covers P_X(i-1) V.
