@@ -43,6 +43,8 @@ PLANTS = {
     "no_max_shift": 5,
     "kv_stride": 6,
     "window_narrow": 7,
+    "ring_offset": 8,
+    "qkv_stride": 9,
 }
 
 
@@ -78,6 +80,10 @@ def _load():
             dp, dp, dp, i64, i64, i32, i32, i32, i32, ctypes.c_double,
             ctypes.POINTER(ctypes.c_int64), ctypes.POINTER(ctypes.c_int32), i64, dp, i32]
         lib.pfa_oracle_prefill_attention_rows.restype = i32
+        lib.pfa_oracle_prefill_attention_cache.argtypes = [
+            dp, dp, dp, dp, i64, i64, i32, i32, i32, i32, ctypes.c_double, i64, i64, i32, i32,
+            i32]
+        lib.pfa_oracle_prefill_attention_cache.restype = i32
         _lib = lib
         return lib
 
@@ -156,6 +162,45 @@ def prefill_attention_rows(q, k, v, rows, window: int = 0, scale: float | None =
         rt.ctypes.data_as(ctypes.POINTER(ctypes.c_int64)),
         rh.ctypes.data_as(ctypes.POINTER(ctypes.c_int32)), len(rows), _ptr(out),
         threads or default_threads())
+    if rc != 0:
+        raise ValueError(f"oracle rejected the arguments (status {rc})")
+    return out
+
+
+def prefill_attention_cache(q_buf, k_buf, v_buf, T: int, start_pos: int, H: int, Hkv: int,
+                            D: int, window: int = 0, scale: float | None = None,
+                            qkv_dim: int | None = None, max_seq_len: int | None = None,
+                            ring: bool = False, out_init=None, threads: int | None = None,
+                            plant: str | None = None) -> np.ndarray:
+    """fp64 attention over caller-layout buffers (flat arrays).
+
+    q_buf holds token t's head h at [t*qkv_dim + h*D, +D); k_buf/v_buf hold
+    key j of kv head kh at [kh*max_seq_len*D + row(j)*D, +D) with row(j) = j,
+    or j % max_seq_len for a circular cache (``ring``).  Returns a flat
+    float64 array of T*qkv_dim elements: the head elements of each row are
+    the attention output, the others are copied from ``out_init`` (NaN when
+    it is None).
+    """
+    qkv_dim = H * D if qkv_dim is None else int(qkv_dim)
+    max_seq_len = start_pos + T if max_seq_len is None else int(max_seq_len)
+    q, k, v = _f64(q_buf).reshape(-1), _f64(k_buf).reshape(-1), _f64(v_buf).reshape(-1)
+    if T > 0 and q.size < (T - 1) * qkv_dim + H * D:
+        raise ValueError("q buffer too small for T rows of qkv_dim")
+    if k.size < Hkv * max_seq_len * D or v.size != k.size:
+        raise ValueError("k/v buffers too small for num_kv_heads * max_seq_len rows")
+    if scale is None:
+        scale = float(np.float32(1.0) / np.sqrt(np.float32(D)))
+    if out_init is None:
+        out = np.full(T * qkv_dim, np.nan, dtype=np.float64)
+    else:
+        out = _f64(out_init).reshape(-1).copy()
+        if out.size != T * qkv_dim:
+            raise ValueError("out_init must hold T * qkv_dim elements")
+    lib = _load()
+    rc = lib.pfa_oracle_prefill_attention_cache(
+        _ptr(q), _ptr(k), _ptr(v), _ptr(out), T, start_pos, H, Hkv, D, int(window),
+        float(scale), qkv_dim, max_seq_len, 1 if ring else 0, threads or default_threads(),
+        PLANTS[plant] if plant else 0)
     if rc != 0:
         raise ValueError(f"oracle rejected the arguments (status {rc})")
     return out

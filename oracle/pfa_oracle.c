@@ -22,9 +22,18 @@
  *   w_j   = exp(s_j - max_j s_j)
  *   out[t][h][d] = sum_j w_j * v[kh][j][d] / sum_j w_j
  *
- * Layouts (row-major, contiguous):
+ * Layouts (row-major):
  *   q, out : [T][H][D]          (token-major, as the page's batch_q / batch_xb)
  *   k, v   : [Hkv][L][D]        (one contiguous [L x D] block per kv head)
+ *
+ * The cache-layout entry point reads the same quantities from the strided
+ * buffers the gnosis page describes in section "GPU design", "Layout":
+ *   q[t][h][d]   at q[t * qkv_dim + h * D + d]       (batch_q rows of qkv_dim)
+ *   out[t][h][d] at out[t * qkv_dim + h * D + d]     (batch_xb rows)
+ *   k[kh][j][d]  at k[kh * max_seq_len * D + row(j) * D + d]
+ * with row(j) = j for a linear cache and row(j) = j mod max_seq_len for a
+ * circular one (the sliding-window layers of the TensorSharp2 Gemma-4 prefill
+ * design write position pos at index pos % capacity, section 4, R4).
  *
  * Everything is computed in double.  Each (t, h) row is computed by exactly
  * one thread in a fixed serial order, so the result does not depend on the
@@ -48,7 +57,9 @@ enum {
     PLANT_NO_SCALE = 4,         /* scale not applied                               */
     PLANT_NO_MAX_SHIFT = 5,     /* exp(s_j) without subtracting the row maximum    */
     PLANT_KV_STRIDE = 6,        /* kv head block stride taken as T*D, not L*D      */
-    PLANT_WINDOW_NARROW = 7     /* window band one key too narrow                  */
+    PLANT_WINDOW_NARROW = 7,    /* window band one key too narrow                  */
+    PLANT_RING_OFFSET = 8,      /* circular cache row (j + 1) mod capacity         */
+    PLANT_QKV_STRIDE = 9        /* q rows taken as H*D apart instead of qkv_dim    */
 };
 
 typedef struct {
@@ -58,6 +69,9 @@ typedef struct {
     int H, Hkv, D, window;
     double scale;
     int plant;
+    /* layout: element strides of q/out rows and of kv heads, circular cache */
+    int64_t qkv_dim, max_seq_len;
+    int ring;
     /* rows to compute: either all T*H rows (row_t == NULL) or a list */
     const int64_t *row_t;
     const int32_t *row_h;
@@ -65,6 +79,14 @@ typedef struct {
     int nthreads, tid;
     int failed;
 } job_t;
+
+/* Cache row that holds key position j. */
+static int64_t key_row(const job_t *J, int64_t j)
+{
+    if (!J->ring) return j;
+    if (J->plant == PLANT_RING_OFFSET) return (j + 1) % J->max_seq_len;
+    return j % J->max_seq_len;
+}
 
 /* One output row: out_row[0..D) = attention of query (t, h). */
 static int attend_row(const job_t *J, int64_t t, int h, double *out_row, double *s)
@@ -93,8 +115,9 @@ static int attend_row(const job_t *J, int64_t t, int h, double *out_row, double 
     }
 
     const int64_t kv_stride = (J->plant == PLANT_KV_STRIDE) ? J->T * (int64_t)J->D
-                                                            : L * (int64_t)J->D;
-    const double *qr = J->q + (t * J->H + h) * (int64_t)J->D;
+                                                            : J->max_seq_len * (int64_t)J->D;
+    const int64_t q_stride = (J->plant == PLANT_QKV_STRIDE) ? (int64_t)J->H * J->D : J->qkv_dim;
+    const double *qr = J->q + t * q_stride + h * (int64_t)J->D;
     const double *kb = J->k + kh * kv_stride;
     const double *vb = J->v + kh * kv_stride;
     const double scale = (J->plant == PLANT_NO_SCALE) ? 1.0 : J->scale;
@@ -102,7 +125,7 @@ static int attend_row(const job_t *J, int64_t t, int h, double *out_row, double 
     /* scores */
     double m = -INFINITY;
     for (int64_t j = lo; j <= hi; ++j) {
-        const double *kr = kb + j * J->D;
+        const double *kr = kb + key_row(J, j) * J->D;
         double dot = 0.0;
         for (int d = 0; d < J->D; ++d) dot += qr[d] * kr[d];
         s[j - lo] = scale * dot;
@@ -116,7 +139,7 @@ static int attend_row(const job_t *J, int64_t t, int h, double *out_row, double 
     for (int64_t j = lo; j <= hi; ++j) {
         const double w = exp(s[j - lo] - m);
         Z += w;
-        const double *vr = vb + j * J->D;
+        const double *vr = vb + key_row(J, j) * J->D;
         for (int d = 0; d < J->D; ++d) out_row[d] += w * vr[d];
     }
     for (int d = 0; d < J->D; ++d) out_row[d] /= Z;
@@ -138,7 +161,7 @@ static void *worker(void *arg)
             dst = J->out + r * (int64_t)J->D;
         } else {
             t = r / J->H; h = (int)(r % J->H);
-            dst = J->out + r * (int64_t)J->D;     /* [T][H][D] flat index (t*H+h)*D */
+            dst = J->out + t * J->qkv_dim + h * (int64_t)J->D;   /* [T][H][D] when qkv_dim = H*D */
         }
         attend_row(J, t, h, dst, s);
     }
@@ -189,6 +212,7 @@ int pfa_oracle_prefill_attention_planted(const double *q, const double *k, const
     J.q = q; J.k = k; J.v = v; J.out = out;
     J.T = T; J.start_pos = start_pos; J.H = H; J.Hkv = Hkv; J.D = D;
     J.window = window; J.scale = scale; J.plant = plant; J.nthreads = nthreads;
+    J.qkv_dim = (int64_t)H * D; J.max_seq_len = start_pos + T; J.ring = 0;
     return run(&J);
 }
 
@@ -219,6 +243,40 @@ int pfa_oracle_prefill_attention_rows(const double *q, const double *k, const do
     J.q = q; J.k = k; J.v = v; J.out = out_rows;
     J.T = T; J.start_pos = start_pos; J.H = H; J.Hkv = Hkv; J.D = D;
     J.window = window; J.scale = scale; J.plant = PLANT_NONE; J.nthreads = nthreads;
+    J.qkv_dim = (int64_t)H * D; J.max_seq_len = start_pos + T; J.ring = 0;
     J.row_t = row_t; J.row_h = row_h; J.nrows = nrows;
+    return run(&J);
+}
+
+/*
+ * Cache layout (see the header comment): q and out rows qkv_dim elements
+ * apart, max_seq_len rows per kv head, key j in row j (ring == 0, needs
+ * max_seq_len >= L) or in row j mod max_seq_len (ring != 0, needs window > 0
+ * and max_seq_len >= min(L, window + T - 1): every key some row of the chunk
+ * sees is still in the cache).  Only the H*D head elements of each out row
+ * are written.
+ */
+int pfa_oracle_prefill_attention_cache(const double *q, const double *k, const double *v,
+                                       double *out, int64_t T, int64_t start_pos,
+                                       int H, int Hkv, int D, int window, double scale,
+                                       int64_t qkv_dim, int64_t max_seq_len, int ring,
+                                       int nthreads, int plant)
+{
+    int rc = check_args(q, k, v, out, T, start_pos, H, Hkv, D);
+    if (rc) return rc;
+    const int64_t L = start_pos + T;
+    if (qkv_dim < (int64_t)H * D || max_seq_len <= 0) return -2;
+    if (!ring && max_seq_len < L) return -2;
+    if (ring) {
+        if (window <= 0) return -2;
+        const int64_t span = (window + T - 1 < L) ? window + T - 1 : L;
+        if (max_seq_len < span) return -2;
+    }
+    if (T == 0) return 0;
+    job_t J = {0};
+    J.q = q; J.k = k; J.v = v; J.out = out;
+    J.T = T; J.start_pos = start_pos; J.H = H; J.Hkv = Hkv; J.D = D;
+    J.window = window; J.scale = scale; J.plant = plant; J.nthreads = nthreads;
+    J.qkv_dim = qkv_dim; J.max_seq_len = max_seq_len; J.ring = ring ? 1 : 0;
     return run(&J);
 }
