@@ -21,8 +21,8 @@ import torch
 from . import _binding
 from ._binding import PFA_BF16, PFA_F32, PfaError
 
-__all__ = ["prefill_attention", "workspace_bytes", "last_device_error", "status_string", "version",
-           "debug_configure", "PfaError", "PFA_F32", "PFA_BF16"]
+__all__ = ["prefill_attention", "prefill_attention_cache", "workspace_bytes", "last_device_error",
+           "status_string", "version", "debug_configure", "PfaError", "PFA_F32", "PFA_BF16"]
 
 _DTYPES = {torch.float32: PFA_F32, torch.bfloat16: PFA_BF16}
 
@@ -135,6 +135,72 @@ def prefill_attention(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Ten
             return out
         return od.to("cpu")
     return od
+
+
+def prefill_attention_cache(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor,
+                            out: torch.Tensor | None = None, *, start_pos: int, window: int = 0,
+                            scale: float | None = None, ring: bool = False, stream=None,
+                            workspace="auto") -> torch.Tensor:
+    """Prefill attention on the caller's buffer layout (pfa_prefill_attention_cache).
+
+    q: [T, H, D] CUDA tensor whose heads and elements are dense (strides
+    (qkv_dim, D, 1), e.g. a column slice of a [T, qkv_dim] projection
+    buffer); out: None (allocated with q's strides) or a tensor with q's
+    shape and strides, of which only the head elements are written.
+    k_cache, v_cache: the whole cache allocation, contiguous
+    [Hkv, max_seq_len, D]; key j of the sequence is in row j, or in row
+    j % max_seq_len when ``ring`` (a circular sliding-window cache; then
+    window > 0 and max_seq_len >= min(L, window + T - 1)).  start_pos is
+    required.  Other arguments: as for prefill_attention.
+    """
+    if q.dim() != 3 or k_cache.dim() != 3 or v_cache.dim() != 3:
+        raise ValueError("q must be [T, H, D]; k_cache and v_cache [Hkv, max_seq_len, D]")
+    if k_cache.shape != v_cache.shape:
+        raise ValueError("k_cache and v_cache shapes differ")
+    if q.dtype not in _DTYPES or k_cache.dtype != q.dtype or v_cache.dtype != q.dtype:
+        raise ValueError("q, k_cache and v_cache must all be float32 or all bfloat16")
+    if q.device.type != "cuda" or k_cache.device != q.device or v_cache.device != q.device:
+        raise ValueError("q, k_cache and v_cache must be CUDA tensors on one device")
+    T, H, D = q.shape
+    Hkv, max_seq_len, Dk = k_cache.shape
+    if Dk != D:
+        raise ValueError("head_dim of q and the cache differ")
+    if q.stride(2) != 1 or (H > 1 and q.stride(1) != D):
+        raise ValueError("q's heads and elements must be dense (strides (qkv_dim, D, 1))")
+    qkv_dim = q.stride(0) if T > 1 else H * D
+    if not (k_cache.is_contiguous() and v_cache.is_contiguous()):
+        raise ValueError("k_cache and v_cache must be contiguous allocations")
+    if out is None:
+        out = torch.empty_strided(q.shape, q.stride(), dtype=q.dtype, device=q.device)
+    if (out.shape != q.shape or out.dtype != q.dtype or out.device != q.device
+            or (T > 1 and out.stride() != q.stride())):
+        raise ValueError("out must match q in shape, strides, dtype and device")
+    if scale is None:
+        scale = float(torch.tensor(1.0 / math.sqrt(D), dtype=torch.float32))
+    dev = q.device
+    lib = _binding.load()
+    with torch.cuda.device(dev):
+        st = _stream_handle(dev, stream)
+        ws_ptr, ws_bytes = None, 0
+        if isinstance(workspace, str):
+            if workspace != "auto":
+                raise ValueError("workspace must be 'auto', None or a uint8 CUDA tensor")
+            need = workspace_bytes(T, start_pos, H, Hkv, D, window, q.dtype) if T > 0 else 0
+            workspace = torch.empty(need, dtype=torch.uint8, device=dev) if need > 0 else None
+        if workspace is not None:
+            if workspace.device != dev or workspace.dtype != torch.uint8:
+                raise ValueError("workspace must be a uint8 tensor on the output's device")
+            ws_ptr, ws_bytes = workspace.data_ptr(), workspace.numel()
+        rc = lib.pfa_prefill_attention_cache(
+            q.data_ptr(), k_cache.data_ptr(), v_cache.data_ptr(), out.data_ptr(), int(T),
+            int(start_pos), int(H), int(Hkv), int(D), int(window), float(scale),
+            _DTYPES[q.dtype], int(qkv_dim), int(max_seq_len), 1 if ring else 0, ws_ptr,
+            ws_bytes, st)
+        if workspace is not None and stream is not None:
+            workspace.record_stream(stream)
+    if rc != 0:
+        raise PfaError(rc, "pfa_prefill_attention_cache")
+    return out
 
 
 def last_device_error(stream=None, device=None) -> int:

@@ -22,8 +22,8 @@ STATUS = {
     -7: "PFA_ERR_TIMEOUT", -8: "PFA_ERR_VALUE", -9: "PFA_ERR_ALIAS", -10: "PFA_ERR_SCRATCH",
 }
 EXPORTS = ("pfa_prefill_attention", "pfa_prefill_attention_ws", "pfa_workspace_bytes",
-           "pfa_prefill_attention_noalloc", "pfa_status_string", "pfa_last_device_error",
-           "pfa_version", "pfa_debug_configure")
+           "pfa_prefill_attention_noalloc", "pfa_prefill_attention_cache", "pfa_status_string",
+           "pfa_last_device_error", "pfa_version", "pfa_debug_configure")
 
 _lock = threading.Lock()
 _lib = None
@@ -62,6 +62,10 @@ def load(path: str | None = None) -> ctypes.CDLL:
         lib.pfa_prefill_attention_noalloc.argtypes = [vp, vp, vp, vp, i64, i64, i32, i32, i32,
                                                       i32, ctypes.c_float, i32, vp]
         lib.pfa_prefill_attention_noalloc.restype = i32
+        lib.pfa_prefill_attention_cache.argtypes = [vp, vp, vp, vp, i64, i64, i32, i32, i32,
+                                                    i32, ctypes.c_float, i32, i64, i64, i32, vp,
+                                                    sz, vp]
+        lib.pfa_prefill_attention_cache.restype = i32
         lib.pfa_status_string.argtypes = [i32]
         lib.pfa_status_string.restype = ctypes.c_char_p
         lib.pfa_last_device_error.argtypes = [vp]

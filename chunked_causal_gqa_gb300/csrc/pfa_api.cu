@@ -11,6 +11,7 @@
 
 #include "../../include/pfa.h"
 
+#include <algorithm>
 #include <cmath>
 #include <cstdio>
 #include <cstdlib>
@@ -214,11 +215,29 @@ int pfa_debug_configure(double wait_limit_ms, int force_timeout) {
 
 namespace pfa {
 
+// Bytes spanned by q (or out) and by each of k_cache / v_cache in a layout.
+void layout_spans(int64_t T, int num_heads, int num_kv_heads, int head_dim, int dtype,
+                  int64_t qkv_dim, int64_t max_seq_len, size_t* qo_bytes, size_t* kv_bytes) {
+  const size_t es = dtype == PFA_F32 ? 4 : 2;
+  *qo_bytes = ((size_t)(T - 1) * (size_t)qkv_dim + (size_t)num_heads * head_dim) * es;
+  *kv_bytes = (size_t)num_kv_heads * (size_t)max_seq_len * head_dim * es;
+}
+
 // Validation shared by every entry point.  On success fills *c (without the
 // workspace) and returns PFA_OK; T == 0 returns PFA_OK with c->T == 0.
 int prepare(const void* q, const void* k_cache, const void* v_cache, void* out, int64_t T,
             int64_t start_pos, int num_heads, int num_kv_heads, int head_dim, int window,
             float scale, int dtype, void* stream, bool check_pointers, Call* c) {
+  const int64_t hd = (num_heads > 0 && head_dim > 0) ? (int64_t)num_heads * head_dim : 0;
+  return prepare_layout(q, k_cache, v_cache, out, T, start_pos, num_heads, num_kv_heads,
+                        head_dim, window, scale, dtype, hd, start_pos + T, 0, stream,
+                        check_pointers, c);
+}
+
+int prepare_layout(const void* q, const void* k_cache, const void* v_cache, void* out,
+                   int64_t T, int64_t start_pos, int num_heads, int num_kv_heads, int head_dim,
+                   int window, float scale, int dtype, int64_t qkv_dim, int64_t max_seq_len,
+                   int ring, void* stream, bool check_pointers, Call* c) {
   // ---- pure argument checks (no CUDA calls)
   if (dtype != PFA_F32 && dtype != PFA_BF16) return PFA_ERR_DTYPE;
   if (T < 0 || start_pos < 0 || num_heads <= 0 || num_kv_heads <= 0) return PFA_ERR_SHAPE;
@@ -236,14 +255,28 @@ int prepare(const void* q, const void* k_cache, const void* v_cache, void* out, 
   if (!std::isfinite(scale)) return PFA_ERR_VALUE;
   c->T = T;
   if (T == 0) return PFA_OK;
+  // ---- layout
+  if (qkv_dim < (int64_t)num_heads * head_dim || max_seq_len <= 0 ||
+      max_seq_len > ((int64_t)1 << 31) - 4096)
+    return PFA_ERR_SHAPE;
+  if (!ring && max_seq_len < L) return PFA_ERR_SHAPE;
+  if (ring) {
+    // every key some row of the chunk sees must still be in the cache
+    if (window <= 0) return PFA_ERR_SHAPE;
+    const int64_t span = std::min<int64_t>(L, (int64_t)window + T - 1);
+    if (max_seq_len < span) return PFA_ERR_SHAPE;
+    // a wrapped bf16 ring must not wrap inside a 128-key tile
+    if (dtype == PFA_BF16 && max_seq_len < L && max_seq_len % 128 != 0) return PFA_ERR_SHAPE;
+  }
+  if ((qkv_dim * (dtype == PFA_F32 ? 4 : 2)) % 16 != 0) return PFA_ERR_ALIGNMENT;
   if (check_pointers) {
     if (!q || !k_cache || !v_cache || !out) return PFA_ERR_NULL;
     const uintptr_t mis = reinterpret_cast<uintptr_t>(q) | reinterpret_cast<uintptr_t>(k_cache) |
                           reinterpret_cast<uintptr_t>(v_cache) | reinterpret_cast<uintptr_t>(out);
     if (mis & 15u) return PFA_ERR_ALIGNMENT;
-    const size_t es = dtype == PFA_F32 ? 4 : 2;
-    const size_t qo_bytes = (size_t)T * num_heads * head_dim * es;
-    const size_t kv_bytes = (size_t)num_kv_heads * (size_t)L * head_dim * es;
+    size_t qo_bytes = 0, kv_bytes = 0;
+    layout_spans(T, num_heads, num_kv_heads, head_dim, dtype, qkv_dim, max_seq_len, &qo_bytes,
+                 &kv_bytes);
     if (overlaps(out, qo_bytes, q, qo_bytes) || overlaps(out, qo_bytes, k_cache, kv_bytes) ||
         overlaps(out, qo_bytes, v_cache, kv_bytes))
       return PFA_ERR_ALIAS;
@@ -280,6 +313,27 @@ int prepare(const void* q, const void* k_cache, const void* v_cache, void* out, 
   c->num_sms = st->num_sms;
   c->ws = nullptr;
   c->ws_bytes = 0;
+  c->qkv_dim = qkv_dim;
+  c->max_seq_len = max_seq_len;
+  c->ring = ring ? 1 : 0;
+  return PFA_OK;
+}
+
+// Attaches a caller workspace to a prepared call after checking it.
+int attach_workspace(Call* c, int dtype, void* workspace, size_t workspace_bytes) {
+  if (workspace == nullptr || workspace_bytes == 0) return PFA_OK;
+  if (reinterpret_cast<uintptr_t>(workspace) & 255u) return PFA_ERR_ALIGNMENT;
+  if (!device_accessible(workspace, c->device)) return PFA_ERR_DEVICE;
+  size_t qo_bytes = 0, kv_bytes = 0;
+  layout_spans(c->T, c->H, c->Hkv, c->D, dtype, c->qkv_dim, c->max_seq_len, &qo_bytes,
+               &kv_bytes);
+  if (overlaps(workspace, workspace_bytes, c->out, qo_bytes) ||
+      overlaps(workspace, workspace_bytes, c->q, qo_bytes) ||
+      overlaps(workspace, workspace_bytes, c->k, kv_bytes) ||
+      overlaps(workspace, workspace_bytes, c->v, kv_bytes))
+    return PFA_ERR_ALIAS;
+  c->ws = workspace;
+  c->ws_bytes = workspace_bytes;
   return PFA_OK;
 }
 
@@ -316,23 +370,24 @@ int pfa_prefill_attention_ws(const void* q, const void* k_cache, const void* v_c
                              int head_dim, int window, float scale, int dtype, void* workspace,
                              size_t workspace_bytes, void* stream) {
   Call c;
-  const int rc = prepare(q, k_cache, v_cache, out, T, start_pos, num_heads, num_kv_heads,
-                         head_dim, window, scale, dtype, stream, true, &c);
+  int rc = prepare(q, k_cache, v_cache, out, T, start_pos, num_heads, num_kv_heads, head_dim,
+                   window, scale, dtype, stream, true, &c);
   if (rc != PFA_OK || c.T == 0) return rc;
-  if (workspace != nullptr && workspace_bytes > 0) {
-    if (reinterpret_cast<uintptr_t>(workspace) & 255u) return PFA_ERR_ALIGNMENT;
-    if (!device_accessible(workspace, c.device)) return PFA_ERR_DEVICE;
-    const size_t qo_bytes = (size_t)T * num_heads * head_dim * (dtype == PFA_F32 ? 4 : 2);
-    const size_t kv_bytes =
-        (size_t)num_kv_heads * (size_t)(start_pos + T) * head_dim * (dtype == PFA_F32 ? 4 : 2);
-    if (overlaps(workspace, workspace_bytes, out, qo_bytes) ||
-        overlaps(workspace, workspace_bytes, q, qo_bytes) ||
-        overlaps(workspace, workspace_bytes, k_cache, kv_bytes) ||
-        overlaps(workspace, workspace_bytes, v_cache, kv_bytes))
-      return PFA_ERR_ALIAS;
-    c.ws = workspace;
-    c.ws_bytes = workspace_bytes;
-  }
+  if ((rc = attach_workspace(&c, dtype, workspace, workspace_bytes)) != PFA_OK) return rc;
+  return dispatch(c, dtype);
+}
+
+int pfa_prefill_attention_cache(const void* q, const void* k_cache, const void* v_cache,
+                                void* out, int64_t T, int64_t start_pos, int num_heads,
+                                int num_kv_heads, int head_dim, int window, float scale,
+                                int dtype, int64_t qkv_dim, int64_t max_seq_len, int ring,
+                                void* workspace, size_t workspace_bytes, void* stream) {
+  Call c;
+  int rc = prepare_layout(q, k_cache, v_cache, out, T, start_pos, num_heads, num_kv_heads,
+                          head_dim, window, scale, dtype, qkv_dim, max_seq_len, ring, stream,
+                          true, &c);
+  if (rc != PFA_OK || c.T == 0) return rc;
+  if ((rc = attach_workspace(&c, dtype, workspace, workspace_bytes)) != PFA_OK) return rc;
   return dispatch(c, dtype);
 }
 

@@ -135,6 +135,8 @@ struct MergeSched {
 struct Params {
   __nv_bfloat16* out;
   float* ws;  // partial slots (balanced schedule only)
+  int64_t o_stride;  // elements from one token's output row to the next
+  int ring_rows;     // > 0: key j is in cache row j % ring_rows; 0: in row j
   int64_t T, start_pos;
   int H, Hkv, group, tok_per_tile, window, units_per_head;
   float scale_log2;
@@ -244,14 +246,16 @@ bf16_d128_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
         ++nq;
         for (int i = it.kb; i < it.ke && ok; ++i) {
           const int key0 = (int)((u.kt_first + i) * kBN);
+          // A circular cache of a multiple of kBN rows never wraps inside a tile.
+          const int row0 = p.ring_rows > 0 ? key0 % p.ring_rows : key0;
           for (int kv = 0; kv < 2; ++kv) {
             const uint32_t s = li % kSlots, ph = (li / kSlots) & 1u;
             if (!(ok = mbar_wait(bar(kBarEmpty + s), ph ^ 1u, abort_flag, p.err, lim))) break;
             const uint32_t dst = sbase + kSmemRing + s * kTileBytes;
             const CUtensorMap* map = kv ? &tm_v : &tm_k;
             mbar_arrive_expect_tx(bar(kBarFull + s), kTileBytes);
-            tma_load_3d(dst, map, bar(kBarFull + s), 0, key0, u.kh);
-            tma_load_3d(dst + kHalfBytes, map, bar(kBarFull + s), 64, key0, u.kh);
+            tma_load_3d(dst, map, bar(kBarFull + s), 0, row0, u.kh);
+            tma_load_3d(dst + kHalfBytes, map, bar(kBarFull + s), 64, row0, u.kh);
             ++li;
           }
         }
@@ -487,7 +491,7 @@ bf16_d128_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
       if (it.slot < 0) {
         // whole pair: normalise, round to bf16, store token-major
         const float inv = l > 0.f ? 1.f / l : 0.f;
-        __nv_bfloat16* orow = p.out + ((t * p.H + h) * (int64_t)128);
+        __nv_bfloat16* orow = p.out + (t * p.o_stride + h * (int64_t)128);
 #pragma unroll 1
         for (int c0 = 0; c0 < 128; c0 += 32) {
           uint32_t o[32];
@@ -600,7 +604,7 @@ merge_kernel(const Params p, const __grid_constant__ MergeSched ms) {
     wv[2 * q] = pack_bf16x2(acc[q].x * inv, acc[q].y * inv);
     wv[2 * q + 1] = pack_bf16x2(acc[q].z * inv, acc[q].w * inv);
   }
-  uint4* dst = reinterpret_cast<uint4*>(p.out + (t * p.H + h) * (int64_t)128 + cq0 * 4);
+  uint4* dst = reinterpret_cast<uint4*>(p.out + t * p.o_stride + h * (int64_t)128 + cq0 * 4);
 #pragma unroll
   for (int q = 0; q < kMergeCols / 8; ++q)
     dst[q] = make_uint4(wv[4 * q], wv[4 * q + 1], wv[4 * q + 2], wv[4 * q + 3]);
@@ -822,17 +826,17 @@ int launch_bf16_d128(const Call& c) {
     plan->grid = s.pairs;
   }
 
-  const int64_t L = c.start_pos + c.T;
   CUtensorMap tq, tk, tv;
   {
     const uint64_t dims[3] = {128, (uint64_t)c.H, (uint64_t)c.T};
-    const uint64_t strides[2] = {128 * 2, (uint64_t)c.H * 128 * 2};
+    const uint64_t strides[2] = {128 * 2, (uint64_t)c.qkv_dim * 2};
     const uint32_t box[3] = {64, (uint32_t)s.group, (uint32_t)s.tok_per_tile};
     if (encode_tmap_bf16_3d(&tq, c.q, dims, strides, box)) return kErrLaunch;
   }
   {
-    const uint64_t dims[3] = {128, (uint64_t)L, (uint64_t)c.Hkv};
-    const uint64_t strides[2] = {128 * 2, (uint64_t)L * 128 * 2};
+    // Rows past the written part of the cache read as zeros.
+    const uint64_t dims[3] = {128, (uint64_t)cache_rows_written(c), (uint64_t)c.Hkv};
+    const uint64_t strides[2] = {128 * 2, (uint64_t)c.max_seq_len * 128 * 2};
     const uint32_t box[3] = {64, (uint32_t)kBN, 1};
     if (encode_tmap_bf16_3d(&tk, c.k, dims, strides, box)) return kErrLaunch;
     if (encode_tmap_bf16_3d(&tv, c.v, dims, strides, box)) return kErrLaunch;
@@ -840,6 +844,8 @@ int launch_bf16_d128(const Call& c) {
   Params p;
   p.out = static_cast<__nv_bfloat16*>(c.out);
   p.ws = static_cast<float*>(c.ws);
+  p.o_stride = c.qkv_dim;
+  p.ring_rows = ring_rows(c);
   p.T = c.T;
   p.start_pos = c.start_pos;
   p.H = c.H;

@@ -72,6 +72,8 @@ constexpr uint32_t kIdescPV = idesc_bf16_f32(kBM, kDHalf, true);
 
 struct Params {
   __nv_bfloat16* out;
+  int64_t o_stride;  // elements from one token's output row to the next
+  int ring_rows;     // > 0: key j is in cache row j % ring_rows; 0: in row j
   int64_t T, start_pos;
   int H, Hkv, group, tok_per_tile, window, tiles_per_head;
   float scale_log2;
@@ -153,7 +155,8 @@ bf16_d512_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
                                  lim)))
               break;
             mbar_arrive_expect_tx(bar(kBarKFull + c), (uint32_t)kKChunk);
-            tma_load_3d(sbase + kSmemK + c * kKChunk, map, bar(kBarKFull + c), 64 * c, key0, kh);
+            tma_load_3d(sbase + kSmemK + c * kKChunk, map, bar(kBarKFull + c), 64 * c,
+                        p.ring_rows > 0 ? key0 % p.ring_rows : key0, kh);
             ++part;
           }
           if (ok) {
@@ -176,7 +179,7 @@ bf16_d512_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
           mbar_arrive_expect_tx(bar(kBarVFull), (uint32_t)(4 * kKChunk));
           for (int c = 0; c < 4; ++c)
             tma_load_3d(sbase + kSmemV + c * kKChunk, map, bar(kBarVFull), dh * kDHalf + 64 * c,
-                        key0, kh);
+                        p.ring_rows > 0 ? key0 % p.ring_rows : key0, kh);
           ++issued;
         }
         if (issued > 0)
@@ -345,7 +348,7 @@ bf16_d512_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
     if (ok) {
       tc_fence_after();
       const float inv = l > 0.f ? 1.f / l : 0.f;
-      __nv_bfloat16* orow = p.out + ((t * p.H + h) * (int64_t)512 + dh * kDHalf);
+      __nv_bfloat16* orow = p.out + (t * p.o_stride + h * (int64_t)512 + dh * kDHalf);
 #pragma unroll 1
       for (int c0 = 0; c0 < kDHalf; c0 += 32) {
         uint32_t o[32];
@@ -395,19 +398,22 @@ int launch_bf16_d512(const Call& c) {
   CUtensorMap tq, tk, tv;
   {
     const uint64_t dims[3] = {512, (uint64_t)c.H, (uint64_t)c.T};
-    const uint64_t strides[2] = {512 * 2, (uint64_t)c.H * 512 * 2};
+    const uint64_t strides[2] = {512 * 2, (uint64_t)c.qkv_dim * 2};
     const uint32_t box[3] = {64, (uint32_t)group, (uint32_t)tok_per_tile};
     if (encode_tmap_bf16_3d(&tq, c.q, dims, strides, box)) return kErrLaunch;
   }
   {
-    const uint64_t dims[3] = {512, (uint64_t)L, (uint64_t)c.Hkv};
-    const uint64_t strides[2] = {512 * 2, (uint64_t)L * 512 * 2};
+    // Rows past the written part of the cache read as zeros.
+    const uint64_t dims[3] = {512, (uint64_t)cache_rows_written(c), (uint64_t)c.Hkv};
+    const uint64_t strides[2] = {512 * 2, (uint64_t)c.max_seq_len * 512 * 2};
     const uint32_t box[3] = {64, (uint32_t)kBN, 1};
     if (encode_tmap_bf16_3d(&tk, c.k, dims, strides, box)) return kErrLaunch;
     if (encode_tmap_bf16_3d(&tv, c.v, dims, strides, box)) return kErrLaunch;
   }
   Params p;
   p.out = static_cast<__nv_bfloat16*>(c.out);
+  p.o_stride = c.qkv_dim;
+  p.ring_rows = ring_rows(c);
   p.T = c.T;
   p.start_pos = c.start_pos;
   p.H = c.H;

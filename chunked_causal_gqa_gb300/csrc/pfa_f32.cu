@@ -34,6 +34,9 @@ struct F32Params {
   const float* k;
   const float* v;
   float* out;
+  int64_t q_stride;        // elements from one token's q / out row to the next
+  int64_t kv_head_stride;  // elements from one kv head's cache block to the next
+  int64_t ring_rows;       // > 0: key j is in cache row j % ring_rows; 0: in row j
   int64_t T, start_pos, L;
   int H, Hkv, group, D, window;
   float scale_log2;        // scale * log2(e)
@@ -72,7 +75,7 @@ f32_attention_kernel(const F32Params p) {
   const int64_t pos = p.start_pos + t;
 
   for (int d = lane; d < D; d += 32)
-    sQ[warp * D + d] = active ? p.q[(t * p.H + h) * (int64_t)D + d] : 0.f;
+    sQ[warp * D + d] = active ? p.q[t * p.q_stride + h * (int64_t)D + d] : 0.f;
 
   // Keys any row of this block can see.
   const int64_t r_last = min(r0 + kRowsPerBlock, p.rows_per_head) - 1;
@@ -81,8 +84,8 @@ f32_attention_kernel(const F32Params p) {
   const int64_t kmin = p.window > 0 ? max((int64_t)0, pos_lo - p.window + 1) : 0;
   const int64_t kmax = pos_hi;
 
-  const float* kbase = p.k + (int64_t)kh * p.L * D;
-  const float* vbase = p.v + (int64_t)kh * p.L * D;
+  const float* kbase = p.k + (int64_t)kh * p.kv_head_stride;
+  const float* vbase = p.v + (int64_t)kh * p.kv_head_stride;
   const int ncols = (D + 31) >> 5;
 
   float m = -INFINITY, l = 0.f;
@@ -107,8 +110,9 @@ f32_attention_kernel(const F32Params p) {
           const int64_t j = j0 + jj;
           if (j <= kmax) {
             const int d = idx * 4 - jj * D;
-            kr4[u] = *reinterpret_cast<const float4*>(kbase + j * D + d);
-            vr4[u] = *reinterpret_cast<const float4*>(vbase + j * D + d);
+            const int64_t row = p.ring_rows > 0 ? j % p.ring_rows : j;
+            kr4[u] = *reinterpret_cast<const float4*>(kbase + row * D + d);
+            vr4[u] = *reinterpret_cast<const float4*>(vbase + row * D + d);
           }
         }
       }
@@ -162,7 +166,7 @@ f32_attention_kernel(const F32Params p) {
 
   if (active) {
     const float inv = 1.f / l;
-    float* orow = p.out + (t * p.H + h) * (int64_t)D;
+    float* orow = p.out + t * p.q_stride + h * (int64_t)D;
 #pragma unroll
     for (int c = 0; c < kMaxCols; ++c) {
       const int d = lane + 32 * c;
@@ -192,6 +196,9 @@ int launch_f32(const Call& c) {
   p.k = static_cast<const float*>(c.k);
   p.v = static_cast<const float*>(c.v);
   p.out = static_cast<float*>(c.out);
+  p.q_stride = c.qkv_dim;
+  p.kv_head_stride = c.max_seq_len * (int64_t)c.D;
+  p.ring_rows = ring_rows(c);
   p.T = c.T;
   p.start_pos = c.start_pos;
   p.L = c.start_pos + c.T;

@@ -24,7 +24,24 @@ struct Call {
   int num_sms;
   void* ws;               // caller's workspace (device), may be null
   size_t ws_bytes;
+  // Layout (defaults describe the contiguous layout of pfa_prefill_attention):
+  int64_t qkv_dim;        // elements from one token's q / out row to the next (>= H*D)
+  int64_t max_seq_len;    // rows per kv head in k / v (kv head stride = max_seq_len * D)
+  int ring;               // 1: key j lives in row j % max_seq_len (circular cache)
 };
+
+// Rows at the start of each kv head's block that hold written keys: L for a
+// linear cache, min(L, capacity) for a circular one.  Rows past them are
+// never read (TMA reads them as zeros).
+inline int64_t cache_rows_written(const Call& c) {
+  const int64_t L = c.start_pos + c.T;
+  return (c.ring && c.max_seq_len < L) ? c.max_seq_len : L;
+}
+// Modulus of the key -> cache row map once a circular cache has wrapped
+// (L > capacity); 0 means key j is in row j.
+inline int ring_rows(const Call& c) {
+  return (c.ring && c.max_seq_len < c.start_pos + c.T) ? (int)c.max_seq_len : 0;
+}
 
 constexpr int kFlagForceTimeout = 1;
 
@@ -42,6 +59,12 @@ int encode_tmap_bf16_3d(CUtensorMap* out, const void* base, const uint64_t dims[
 int prepare(const void* q, const void* k_cache, const void* v_cache, void* out, int64_t T,
             int64_t start_pos, int num_heads, int num_kv_heads, int head_dim, int window,
             float scale, int dtype, void* stream, bool check_pointers, Call* c);
+// prepare() for a caller-specified layout: q / out rows qkv_dim elements
+// apart, max_seq_len rows per kv head, optionally circular (ring != 0).
+int prepare_layout(const void* q, const void* k_cache, const void* v_cache, void* out,
+                   int64_t T, int64_t start_pos, int num_heads, int num_kv_heads, int head_dim,
+                   int window, float scale, int dtype, int64_t qkv_dim, int64_t max_seq_len,
+                   int ring, void* stream, bool check_pointers, Call* c);
 // Launches the kernel(s) for a prepared call (pfa_api.cu).
 int dispatch(const Call& c, int dtype);
 

@@ -143,6 +143,49 @@ PFA_API int pfa_prefill_attention_ws(const void *q, const void *k_cache, const v
                                      void *stream);
 
 /*
+ * pfa_prefill_attention_cache -- pfa_prefill_attention_ws on the caller's own
+ * buffer layout instead of the contiguous one.  The layouts are those of the
+ * gnosis page "Prefill attention -> GPU: handoff" (section "GPU design",
+ * "Layout": Q rows of qkv_dim elements in batch_q, kv head kh's block at
+ * kh * max_seq_len * head_dim, the output scattered back into rows of
+ * qkv_dim) and the circular cache of sliding-window layers in the
+ * TensorSharp2 Gemma-4 prefill design (section 4, R4: position pos is stored
+ * at index pos % capacity).
+ *
+ *   q        element (t, h, d) at q[t * qkv_dim + h * head_dim + d].
+ *   out      element (t, h, d) at out[t * qkv_dim + h * head_dim + d]; only
+ *            these T * num_heads * head_dim elements are written, the rest of
+ *            each row is left as it was.  out must not overlap q, k_cache or
+ *            v_cache (taken as their full spans).
+ *   k_cache, v_cache
+ *            key j of kv head kh at k_cache[kh * max_seq_len * head_dim +
+ *            row(j) * head_dim + d], row(j) = j (ring == 0) or
+ *            j % max_seq_len (ring != 0).
+ *   qkv_dim  elements from one token's row to the next in q and out;
+ *            >= num_heads * head_dim, and qkv_dim * element size must be a
+ *            multiple of 16 bytes (PFA_ERR_ALIGNMENT otherwise).
+ *   max_seq_len  rows allocated per kv head (> 0).  With ring == 0 it must be
+ *            >= L = start_pos + T (rows past L are never read).
+ *   ring     non-zero: circular cache.  Needs window > 0 and
+ *            max_seq_len >= min(L, window + T - 1), so that every key a row of
+ *            the chunk sees is still stored (the caller has written positions
+ *            start_pos .. L-1 at row(j), overwriting the oldest).  For PFA_BF16,
+ *            once the ring has wrapped (L > max_seq_len) max_seq_len must be a
+ *            multiple of 128, the key-tile height.
+ *   workspace, workspace_bytes  as for pfa_prefill_attention_ws.
+ *
+ * With qkv_dim = num_heads * head_dim, max_seq_len = L and ring = 0 it is
+ * exactly pfa_prefill_attention_ws.  Layout errors return PFA_ERR_SHAPE
+ * (or PFA_ERR_ALIGNMENT) before anything is enqueued.  Ownership, behaviour,
+ * other errors and determinism: as for pfa_prefill_attention_ws.
+ */
+PFA_API int pfa_prefill_attention_cache(const void *q, const void *k_cache, const void *v_cache,
+                                        void *out, int64_t T, int64_t start_pos, int num_heads,
+                                        int num_kv_heads, int head_dim, int window, float scale,
+                                        int dtype, int64_t qkv_dim, int64_t max_seq_len, int ring,
+                                        void *workspace, size_t workspace_bytes, void *stream);
+
+/*
  * pfa_workspace_bytes -- bytes of workspace the balanced schedule needs for
  * this shape on the current device (0 when it would not be used).  Same
  * shape validation as pfa_prefill_attention; no pointers are needed and
