@@ -21,8 +21,9 @@ import torch
 from . import _binding
 from ._binding import PFA_BF16, PFA_F32, PfaError
 
-__all__ = ["prefill_attention", "prefill_attention_cache", "workspace_bytes", "last_device_error",
-           "status_string", "version", "debug_configure", "PfaError", "PFA_F32", "PFA_BF16"]
+__all__ = ["prefill_attention", "prefill_attention_cache", "workspace_bytes", "schedule",
+           "last_device_error", "status_string", "version", "debug_configure", "PfaError",
+           "PFA_F32", "PFA_BF16"]
 
 _DTYPES = {torch.float32: PFA_F32, torch.bfloat16: PFA_BF16}
 
@@ -44,6 +45,23 @@ def workspace_bytes(T: int, start_pos: int, num_heads: int, num_kv_heads: int, h
     if rc != 0:
         raise PfaError(rc, "pfa_workspace_bytes")
     return int(n.value)
+
+
+SCHEDULES = {0: "plain", 1: "balanced", 2: "tail"}
+
+
+def schedule(T: int, start_pos: int, num_heads: int, num_kv_heads: int, head_dim: int,
+             window: int = 0, dtype: torch.dtype = torch.bfloat16) -> tuple:
+    """(schedule name, workspace bytes) the library uses for a shape with a workspace."""
+    import ctypes
+    lib = _binding.load()
+    kind, n = ctypes.c_int(0), ctypes.c_size_t(0)
+    rc = lib.pfa_schedule(int(T), int(start_pos), int(num_heads), int(num_kv_heads),
+                          int(head_dim), int(window), _DTYPES[dtype], ctypes.byref(kind),
+                          ctypes.byref(n))
+    if rc != 0:
+        raise PfaError(rc, "pfa_schedule")
+    return SCHEDULES[kind.value], int(n.value)
 
 
 def prefill_attention(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor,

@@ -22,7 +22,8 @@ STATUS = {
     -7: "PFA_ERR_TIMEOUT", -8: "PFA_ERR_VALUE", -9: "PFA_ERR_ALIAS", -10: "PFA_ERR_SCRATCH",
 }
 EXPORTS = ("pfa_prefill_attention", "pfa_prefill_attention_ws", "pfa_workspace_bytes",
-           "pfa_prefill_attention_noalloc", "pfa_prefill_attention_cache", "pfa_status_string",
+           "pfa_prefill_attention_noalloc", "pfa_prefill_attention_cache", "pfa_schedule",
+           "pfa_status_string",
            "pfa_last_device_error", "pfa_version", "pfa_debug_configure")
 
 _lock = threading.Lock()
@@ -59,6 +60,9 @@ def load(path: str | None = None) -> ctypes.CDLL:
         lib.pfa_workspace_bytes.argtypes = [i64, i64, i32, i32, i32, i32, i32,
                                             ctypes.POINTER(sz)]
         lib.pfa_workspace_bytes.restype = i32
+        lib.pfa_schedule.argtypes = [i64, i64, i32, i32, i32, i32, i32, ctypes.POINTER(i32),
+                                     ctypes.POINTER(sz)]
+        lib.pfa_schedule.restype = i32
         lib.pfa_prefill_attention_noalloc.argtypes = [vp, vp, vp, vp, i64, i64, i32, i32, i32,
                                                       i32, ctypes.c_float, i32, vp]
         lib.pfa_prefill_attention_noalloc.restype = i32

@@ -403,6 +403,20 @@ int pfa_workspace_bytes(int64_t T, int64_t start_pos, int num_heads, int num_kv_
   return PFA_OK;
 }
 
+int pfa_schedule(int64_t T, int64_t start_pos, int num_heads, int num_kv_heads, int head_dim,
+                 int window, int dtype, int* schedule, size_t* workspace_bytes) {
+  if (!schedule || !workspace_bytes) return PFA_ERR_NULL;
+  *schedule = PFA_SCHEDULE_PLAIN;
+  *workspace_bytes = 0;
+  Call c;
+  const int rc = prepare(nullptr, nullptr, nullptr, nullptr, T, start_pos, num_heads,
+                         num_kv_heads, head_dim, window, 1.0f, dtype, nullptr, false, &c);
+  if (rc != PFA_OK || c.T == 0) return rc;
+  if (dtype == PFA_BF16 && head_dim == 128)
+    *workspace_bytes = workspace_bytes_bf16_d128(c, schedule);
+  return PFA_OK;
+}
+
 int pfa_last_device_error(void* stream) {
   int dev = -1;
   DeviceState* st = nullptr;

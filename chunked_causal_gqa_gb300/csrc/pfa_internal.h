@@ -70,8 +70,9 @@ int dispatch(const Call& c, int dtype);
 
 int launch_f32(const Call& c);
 int launch_bf16_d128(const Call& c);
-// Workspace bytes the balanced head_dim-128 schedule needs (0: not used).
-size_t workspace_bytes_bf16_d128(const Call& c);
+// Workspace bytes the head_dim-128 schedule the host picks needs (0: the plain
+// schedule); *schedule (if not null) gets 0 plain, 1 balanced, 2 tail split.
+size_t workspace_bytes_bf16_d128(const Call& c, int* schedule = nullptr);
 int launch_bf16_d512(const Call& c);
 
 }  // namespace pfa

@@ -195,6 +195,26 @@ PFA_API int pfa_workspace_bytes(int64_t T, int64_t start_pos, int num_heads, int
                                 int head_dim, int window, int dtype, size_t *bytes);
 
 /*
+ * pfa_schedule -- which schedule pfa_prefill_attention_ws runs for this shape
+ * on the current device when its workspace is at least *workspace_bytes
+ * (the value pfa_workspace_bytes reports):
+ *   PFA_SCHEDULE_PLAIN     one kernel, one CTA per pair of 128-row query tiles;
+ *   PFA_SCHEDULE_BALANCED  equal-cost runs of key-tile ranges per SM, then a
+ *                          merge kernel (two launches);
+ *   PFA_SCHEDULE_TAIL      the whole waves of pairs run whole and the pairs
+ *                          of the last, partial wave are cut into equal key
+ *                          ranges, then a merge kernel (two launches).
+ * Same validation as pfa_workspace_bytes; nothing is launched.  Returns
+ * PFA_OK and sets both outputs, or an error status.
+ */
+#define PFA_SCHEDULE_PLAIN 0
+#define PFA_SCHEDULE_BALANCED 1
+#define PFA_SCHEDULE_TAIL 2
+PFA_API int pfa_schedule(int64_t T, int64_t start_pos, int num_heads, int num_kv_heads,
+                         int head_dim, int window, int dtype, int *schedule,
+                         size_t *workspace_bytes);
+
+/*
  * pfa_prefill_attention_noalloc -- the call of pfa_prefill_attention_ws with
  * the balanced schedule, for callers that cannot allocate device memory.
  * (The source pages have no counterpart: this is an interface convenience.)

@@ -87,11 +87,17 @@ def test_mistral_layer_full_parity():
     G.check(got, want, "bf16", wl.name)
 
 
+@pytest.mark.parametrize("workspace", ["auto", None])
 @pytest.mark.parametrize("name", ["chunk_64k", "chunk_128k"])
-def test_long_chunk_sampled_parity(name):
+def test_long_chunk_sampled_parity(name, workspace):
+    """Both the schedule the library picks (the tail split) and the plain one."""
+    import chunked_causal_gqa_gb300 as pkg
     wl = W.WORKLOADS[name]
+    if workspace == "auto":
+        assert pkg.workspace_bytes(wl.T, wl.start_pos, wl.num_heads, wl.num_kv_heads,
+                                   wl.head_dim, wl.window) > 0
     q, k, v = W.make_inputs(wl)
-    out = G.run(q, k, v, window=wl.window, scale=wl.scale)
+    out = G.run(q, k, v, window=wl.window, scale=wl.scale, workspace=workspace)
     rows = G.sample_rows(wl.T, wl.num_heads, 24, seed=wl.seeds[0])
     want = oracle.prefill_attention_rows(q, k, v, rows, window=wl.window, scale=wl.scale)
     got = G.to_np(out)[[t for t, _ in rows], [h for _, h in rows]]
@@ -124,8 +130,9 @@ def test_repeated_runs_are_bit_identical_small(D):
     assert len(digests) == 1
 
 
-def test_repeated_runs_are_bit_identical():
-    wl = W.WORKLOADS["mistral_1358"]
+@pytest.mark.parametrize("name", ["mistral_1358", "chunk_64k"])
+def test_repeated_runs_are_bit_identical(name):
+    wl = W.WORKLOADS[name]
     q, k, v = (x.to(G.dev()) for x in W.make_inputs(wl))
     digests = {G.digest(G.run(q, k, v, scale=wl.scale)) for _ in range(5)}
     assert len(digests) == 1
@@ -159,6 +166,7 @@ SCHEDULE_CASES = [
     (16, 2, 128, 64, 5000, 0),
     (8, 2, 128, 40, 3000, 0),
     (8, 2, 128, 700, 3000, 0),
+    (32, 8, 128, 1280, 2000, 0),   # 160 pairs on 152 SMs: the tail split cuts the last 8
 ]
 
 
