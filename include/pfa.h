@@ -230,11 +230,14 @@ PFA_API int pfa_schedule(int64_t T, int64_t start_pos, int num_heads, int num_kv
  * routine is called.
  *
  * Arguments, layouts, ownership and the result: as for pfa_prefill_attention.
- * For bf16 with head_dim 128 it runs the balanced schedule in the static
- * scratch; a shape whose balanced schedule needs more than
- * PFA_NOALLOC_SCRATCH_BYTES is refused with PFA_ERR_SCRATCH before anything
- * is launched.  Shapes that use no workspace (other dtypes or head_dims, or
- * caches too large for the balanced schedule) run as pfa_prefill_attention.
+ * For bf16 with head_dim 128 it runs the schedule pfa_schedule reports (the
+ * balanced or the tail-split one) in the static scratch; a shape whose
+ * schedule needs more than PFA_NOALLOC_SCRATCH_BYTES is refused with
+ * PFA_ERR_SCRATCH before anything is launched (long chunks deep in a
+ * context, whose tail split needs ~92 MiB for a 2048-token chunk of 32
+ * heads, are refused; pfa_prefill_attention runs them with the plain
+ * schedule).  Shapes that use no workspace (other dtypes or head_dims, or
+ * shapes where the plain schedule is picked) run as pfa_prefill_attention.
  *
  * Sharing: every call on a device uses the same scratch and leaves its own
  * partial results in it.  No part of it needs to be zero on entry (a call
