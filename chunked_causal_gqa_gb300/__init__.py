@@ -21,7 +21,8 @@ import torch
 from . import _binding
 from ._binding import PFA_BF16, PFA_F32, PfaError
 
-__all__ = ["prefill_attention", "prefill_attention_cache", "workspace_bytes", "schedule",
+__all__ = ["prefill_attention", "prefill_attention_cache", "prefill_attention_graph",
+           "workspace_bytes", "schedule",
            "last_device_error", "status_string", "version", "debug_configure", "PfaError",
            "PFA_F32", "PFA_BF16"]
 
@@ -218,6 +219,56 @@ def prefill_attention_cache(q: torch.Tensor, k_cache: torch.Tensor, v_cache: tor
             workspace.record_stream(stream)
     if rc != 0:
         raise PfaError(rc, "pfa_prefill_attention_cache")
+    return out
+
+
+def prefill_attention_graph(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor,
+                            out: torch.Tensor, lengths: torch.Tensor, *, window: int = 0,
+                            scale: float | None = None, ring: bool = False,
+                            stream=None) -> torch.Tensor:
+    """Prefill attention whose {T, start_pos} are read on the device (pfa_prefill_attention_graph).
+
+    q, out: [max_T, H, D] CUDA tensors with dense heads (strides (qkv_dim, D, 1));
+    k_cache, v_cache: contiguous [Hkv, max_seq_len, D]; lengths: a CUDA int64
+    tensor of two elements {T, start_pos}, read when the kernel runs -- so a
+    CUDA graph captured around this call replays for any chunk that fits.
+    Rows of out past the run-time T are not written.
+    """
+    if q.dim() != 3 or k_cache.dim() != 3 or v_cache.dim() != 3:
+        raise ValueError("q must be [max_T, H, D]; k_cache and v_cache [Hkv, max_seq_len, D]")
+    if k_cache.shape != v_cache.shape:
+        raise ValueError("k_cache and v_cache shapes differ")
+    if q.dtype not in _DTYPES or k_cache.dtype != q.dtype or v_cache.dtype != q.dtype:
+        raise ValueError("q, k_cache and v_cache must all be float32 or all bfloat16")
+    devs = {t.device for t in (q, k_cache, v_cache, out, lengths)}
+    if len(devs) != 1 or q.device.type != "cuda":
+        raise ValueError("all tensors must be CUDA tensors on one device")
+    if lengths.dtype != torch.int64 or lengths.numel() != 2 or not lengths.is_contiguous():
+        raise ValueError("lengths must be a contiguous int64 tensor {T, start_pos}")
+    max_T, H, D = q.shape
+    Hkv, max_seq_len, Dk = k_cache.shape
+    if Dk != D:
+        raise ValueError("head_dim of q and the cache differ")
+    if q.stride(2) != 1 or (H > 1 and q.stride(1) != D):
+        raise ValueError("q's heads and elements must be dense (strides (qkv_dim, D, 1))")
+    qkv_dim = q.stride(0) if max_T > 1 else H * D
+    if not (k_cache.is_contiguous() and v_cache.is_contiguous()):
+        raise ValueError("k_cache and v_cache must be contiguous allocations")
+    if (out.shape != q.shape or out.dtype != q.dtype
+            or (max_T > 1 and out.stride() != q.stride())):
+        raise ValueError("out must match q in shape, strides and dtype")
+    if scale is None:
+        scale = float(torch.tensor(1.0 / math.sqrt(D), dtype=torch.float32))
+    dev = q.device
+    lib = _binding.load()
+    with torch.cuda.device(dev):
+        rc = lib.pfa_prefill_attention_graph(
+            q.data_ptr(), k_cache.data_ptr(), v_cache.data_ptr(), out.data_ptr(),
+            lengths.data_ptr(), int(max_T), int(H), int(Hkv), int(D), int(window), float(scale),
+            _DTYPES[q.dtype], int(qkv_dim), int(max_seq_len), 1 if ring else 0,
+            _stream_handle(dev, stream))
+    if rc != 0:
+        raise PfaError(rc, "pfa_prefill_attention_graph")
     return out
 
 

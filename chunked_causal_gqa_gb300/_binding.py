@@ -20,9 +20,11 @@ STATUS = {
     0: "PFA_OK", -1: "PFA_ERR_NULL", -2: "PFA_ERR_SHAPE", -3: "PFA_ERR_DTYPE",
     -4: "PFA_ERR_ALIGNMENT", -5: "PFA_ERR_DEVICE", -6: "PFA_ERR_LAUNCH",
     -7: "PFA_ERR_TIMEOUT", -8: "PFA_ERR_VALUE", -9: "PFA_ERR_ALIAS", -10: "PFA_ERR_SCRATCH",
+    -11: "PFA_ERR_LENGTHS",
 }
 EXPORTS = ("pfa_prefill_attention", "pfa_prefill_attention_ws", "pfa_workspace_bytes",
-           "pfa_prefill_attention_noalloc", "pfa_prefill_attention_cache", "pfa_schedule",
+           "pfa_prefill_attention_noalloc", "pfa_prefill_attention_cache",
+           "pfa_prefill_attention_graph", "pfa_schedule",
            "pfa_status_string",
            "pfa_last_device_error", "pfa_version", "pfa_debug_configure")
 
@@ -70,6 +72,9 @@ def load(path: str | None = None) -> ctypes.CDLL:
                                                     i32, ctypes.c_float, i32, i64, i64, i32, vp,
                                                     sz, vp]
         lib.pfa_prefill_attention_cache.restype = i32
+        lib.pfa_prefill_attention_graph.argtypes = [vp, vp, vp, vp, vp, i64, i32, i32, i32,
+                                                    i32, ctypes.c_float, i32, i64, i64, i32, vp]
+        lib.pfa_prefill_attention_graph.restype = i32
         lib.pfa_status_string.argtypes = [i32]
         lib.pfa_status_string.restype = ctypes.c_char_p
         lib.pfa_last_device_error.argtypes = [vp]

@@ -200,6 +200,8 @@ const char* pfa_status_string(int status) {
     case PFA_ERR_ALIAS: return "PFA_ERR_ALIAS: out overlaps an input";
     case PFA_ERR_SCRATCH:
       return "PFA_ERR_SCRATCH: the shape needs more scratch than the allocation-free entry holds";
+    case PFA_ERR_LENGTHS:
+      return "PFA_ERR_LENGTHS: the device-side {T, start_pos} did not fit the graph call's capacities";
     default: return "PFA: unknown status";
   }
 }
@@ -316,6 +318,7 @@ int prepare_layout(const void* q, const void* k_cache, const void* v_cache, void
   c->qkv_dim = qkv_dim;
   c->max_seq_len = max_seq_len;
   c->ring = ring ? 1 : 0;
+  c->lens = nullptr;
   return PFA_OK;
 }
 
@@ -391,6 +394,28 @@ int pfa_prefill_attention_cache(const void* q, const void* k_cache, const void* 
   return dispatch(c, dtype);
 }
 
+int pfa_prefill_attention_graph(const void* q, const void* k_cache, const void* v_cache,
+                                void* out, const int64_t* lengths, int64_t max_T,
+                                int num_heads, int num_kv_heads, int head_dim, int window,
+                                float scale, int dtype, int64_t qkv_dim, int64_t max_seq_len,
+                                int ring, void* stream) {
+  if (!lengths) return PFA_ERR_NULL;
+  if (reinterpret_cast<uintptr_t>(lengths) & 7u) return PFA_ERR_ALIGNMENT;
+  // The host knows only the capacities: validate as a chunk of max_T tokens
+  // at position 0 (so max_T <= max_seq_len); the kernels check the run-time
+  // values against the same limits.
+  Call c;
+  const int rc = prepare_layout(q, k_cache, v_cache, out, max_T, 0, num_heads, num_kv_heads,
+                                head_dim, window, scale, dtype, qkv_dim, max_seq_len, ring,
+                                stream, true, &c);
+  if (rc != PFA_OK || c.T == 0) return rc;
+  // a bf16 ring may wrap at run time: it must wrap on 128-key tile boundaries
+  if (ring && dtype == PFA_BF16 && max_seq_len % 128 != 0) return PFA_ERR_SHAPE;
+  if (!device_accessible(lengths, c.device)) return PFA_ERR_DEVICE;
+  c.lens = lengths;
+  return dispatch(c, dtype);
+}
+
 int pfa_workspace_bytes(int64_t T, int64_t start_pos, int num_heads, int num_kv_heads,
                         int head_dim, int window, int dtype, size_t* bytes) {
   if (!bytes) return PFA_ERR_NULL;
@@ -434,7 +459,9 @@ int pfa_last_device_error(void* stream) {
     cudaGetLastError();
     return PFA_ERR_DEVICE;
   }
-  return (word & kErrTimeout) ? PFA_ERR_TIMEOUT : PFA_OK;
+  if (word & kErrTimeout) return PFA_ERR_TIMEOUT;
+  if (word & kErrLengths) return PFA_ERR_LENGTHS;
+  return PFA_OK;
 }
 
 }  // extern "C"

@@ -151,7 +151,9 @@ struct Params {
   float* ws;  // partial slots (balanced schedule only)
   int64_t o_stride;  // elements from one token's output row to the next
   int ring_rows;     // > 0: key j is in cache row j % ring_rows; 0: in row j
-  int64_t T, start_pos;
+  int64_t T, start_pos;          // graph entry: T = the largest T, start_pos unused
+  const int64_t* lens;           // graph entry: device {T, start_pos}; else null
+  int64_t kv_capacity;           // rows per kv head in the cache
   int H, Hkv, group, tok_per_tile, window, units_per_head;
   float scale_log2;
   unsigned* err;
@@ -187,7 +189,7 @@ __device__ __forceinline__ Unit unit_of(const Params& p, int pidx) {
   return unit_of(p.T, p.start_pos, p.Hkv, p.tok_per_tile, p.window, p.units_per_head, pidx);
 }
 
-template <bool kFoldScale>
+template <bool kFoldScale, bool kDyn>
 __global__ void __launch_bounds__(kThreads, 1)
 bf16_d128_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                  const __grid_constant__ CUtensorMap tm_v, const Params p,
@@ -204,6 +206,23 @@ bf16_d128_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const uint64_t lim = p.wait_limit_ns;
   const int cta = blockIdx.x;
+  // Chunk length and position: kernel parameters, or (graph entry, kDyn) read
+  // from device memory at run time, with the grid sized for the largest T.
+  int64_t T = p.T, start_pos = p.start_pos;
+  int units_per_head = p.units_per_head;
+  if (kDyn) {
+    T = p.lens[0];
+    start_pos = p.lens[1];
+    if (!lengths_ok(T, start_pos, p.T, p.kv_capacity, p.ring_rows, p.window)) {
+      if (cta == 0 && threadIdx.x == 0) atomicOr(p.err, kErrLengths);
+      return;
+    }
+    units_per_head = (int)(((T + p.tok_per_tile - 1) / p.tok_per_tile + 1) / 2);
+    if (cta >= units_per_head * p.Hkv) return;  // the whole CTA: nothing set up yet
+  }
+  auto unit = [&](int pidx) -> Unit {
+    return unit_of(T, start_pos, p.Hkv, p.tok_per_tile, p.window, units_per_head, pidx);
+  };
   const bool table = (sched.mode == kTable);
   const int item_begin = table ? sched.cta_first[cta] : 0;
   const int item_end = table ? sched.cta_first[cta + 1] : 1;
@@ -213,14 +232,14 @@ bf16_d128_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
     if (sched.mode == kTail && cta >= sched.p1) {
       const int j = cta - sched.p1, r = j / sched.p2;
       it.pair = sched.p1 + j % sched.p2;
-      const int n = unit_of(p, it.pair).n;
+      const int n = unit(it.pair).n;
       it.kb = (int)((int64_t)n * r / sched.parts);
       it.ke = (int)((int64_t)n * (r + 1) / sched.parts);
       it.slot = j;
     } else {
       it.pair = cta;
       it.kb = 0;
-      it.ke = unit_of(p, cta).n;
+      it.ke = unit(cta).n;
       it.slot = -1;
     }
     return it;
@@ -257,7 +276,7 @@ bf16_d128_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
       bool ok = true;
       for (int k = item_begin; k < item_end && ok; ++k) {
         const Item it = get_item(k);
-        const Unit u = unit_of(p, it.pair);
+        const Unit u = unit(it.pair);
         if (nq > 0 && !(ok = mbar_wait(bar(kBarQFree), (nq - 1) & 1u, abort_flag, p.err, lim)))
           break;
         const int hq = u.kh * p.group;
@@ -391,11 +410,11 @@ bf16_d128_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
     uint32_t gi = 0, kk = 0;
     for (int k = item_begin; k < item_end && ok; ++k, ++kk) {
       const Item it = get_item(k);
-      const Unit u = unit_of(p, it.pair);
+      const Unit u = unit(it.pair);
       const int n = it.ke - it.kb;
       // Positions and key indices fit in 32 bits (L < 2^31 - 4096).
       const int t0 = (int)(X ? u.t0B : u.t0A);
-      const int pos_first = (int)p.start_pos + t0;
+      const int pos_first = (int)start_pos + t0;
       // first key of this item's first tile, relative to the row's position
       int key_rel = (int)(u.kt_first + it.kb) * kBN - (pos_first + tok);
 
@@ -510,7 +529,7 @@ bf16_d128_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
       if (!(ok = __all_sync(0xffffffffu, ok))) break;
       tc_fence_after();
       const int64_t t = (int64_t)t0 + tok;
-      const bool row_valid = row_exists && t < p.T;
+      const bool row_valid = row_exists && t < T;
       const int h = u.kh * p.group + hrow;
       if (it.slot < 0) {
         // whole pair: normalise, round to bf16, store token-major
@@ -929,8 +948,10 @@ int launch_bf16_d128(const Call& c) {
   static int attr_state[64] = {0};  // 0: not checked, 1: ok, -1: unusable
   if (c.device < 0 || c.device >= 64) return kErrDevice;
   if (attr_state[c.device] == 0) {
-    const bool ok = setup_kernel((const void*)bf16_d128_kernel<true>) == kOk &&
-                    setup_kernel((const void*)bf16_d128_kernel<false>) == kOk;
+    const bool ok = setup_kernel((const void*)bf16_d128_kernel<true, false>) == kOk &&
+                    setup_kernel((const void*)bf16_d128_kernel<false, false>) == kOk &&
+                    setup_kernel((const void*)bf16_d128_kernel<true, true>) == kOk &&
+                    setup_kernel((const void*)bf16_d128_kernel<false, true>) == kOk;
     attr_state[c.device] = ok ? 1 : -1;
   }
   if (attr_state[c.device] != 1) {
@@ -942,7 +963,7 @@ int launch_bf16_d128(const Call& c) {
 
   // The schedule tables are ~20 KB: built per call on the heap.
   std::unique_ptr<Plan> plan(new Plan());
-  if (!(c.ws != nullptr && choose_schedule(s, c.num_sms, plan.get()) &&
+  if (!(c.ws != nullptr && c.lens == nullptr && choose_schedule(s, c.num_sms, plan.get()) &&
         plan->ws_bytes <= c.ws_bytes)) {
     plan->balanced = false;
     plan->sched.mode = kPlain;
@@ -971,6 +992,8 @@ int launch_bf16_d128(const Call& c) {
   p.ring_rows = ring_rows(c);
   p.T = c.T;
   p.start_pos = c.start_pos;
+  p.lens = c.lens;
+  p.kv_capacity = c.max_seq_len;
   p.H = c.H;
   p.Hkv = c.Hkv;
   p.group = s.group;
@@ -982,10 +1005,21 @@ int launch_bf16_d128(const Call& c) {
   p.wait_limit_ns = c.wait_limit_ns;
   p.flags = c.flags;
   const dim3 grid((unsigned)plan->grid);
-  if (p.scale_log2 > 0.f)
-    bf16_d128_kernel<true><<<grid, kThreads, kSmemAlloc, c.stream>>>(tq, tk, tv, p, plan->sched);
-  else
-    bf16_d128_kernel<false><<<grid, kThreads, kSmemAlloc, c.stream>>>(tq, tk, tv, p, plan->sched);
+  const bool fold = p.scale_log2 > 0.f;
+  if (c.lens) {
+    if (fold)
+      bf16_d128_kernel<true, true><<<grid, kThreads, kSmemAlloc, c.stream>>>(tq, tk, tv, p,
+                                                                           plan->sched);
+    else
+      bf16_d128_kernel<false, true><<<grid, kThreads, kSmemAlloc, c.stream>>>(tq, tk, tv, p,
+                                                                            plan->sched);
+  } else if (fold) {
+    bf16_d128_kernel<true, false><<<grid, kThreads, kSmemAlloc, c.stream>>>(tq, tk, tv, p,
+                                                                          plan->sched);
+  } else {
+    bf16_d128_kernel<false, false><<<grid, kThreads, kSmemAlloc, c.stream>>>(tq, tk, tv, p,
+                                                                           plan->sched);
+  }
   if (cudaGetLastError() != cudaSuccess) return kErrLaunch;
   if (plan->balanced && plan->merge.num > 0) {
     merge_kernel<<<dim3((unsigned)plan->merge.num, 128 / kMergeCols), kPairRows, 0,

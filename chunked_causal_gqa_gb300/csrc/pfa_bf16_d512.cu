@@ -74,7 +74,9 @@ struct Params {
   __nv_bfloat16* out;
   int64_t o_stride;  // elements from one token's output row to the next
   int ring_rows;     // > 0: key j is in cache row j % ring_rows; 0: in row j
-  int64_t T, start_pos;
+  int64_t T, start_pos;          // graph entry: T = the largest T, start_pos unused
+  const int64_t* lens;           // graph entry: device {T, start_pos}; else null
+  int64_t kv_capacity;           // rows per kv head in the cache
   int H, Hkv, group, tok_per_tile, window, tiles_per_head;
   float scale_log2;
   unsigned* err;
@@ -82,7 +84,7 @@ struct Params {
   int flags;
 };
 
-template <bool kFoldScale>
+template <bool kFoldScale, bool kDyn>
 __global__ void __launch_bounds__(kThreads, 1)
 bf16_d512_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                  const __grid_constant__ CUtensorMap tm_v, const Params p) {
@@ -98,18 +100,33 @@ bf16_d512_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const uint64_t lim = p.wait_limit_ns;
 
+  // Chunk length and position: kernel parameters, or (graph entry, kDyn) read
+  // from device memory at run time, with the grid sized for the largest T.
+  int64_t T = p.T, start_pos = p.start_pos;
+  int tiles_per_head = p.tiles_per_head;
+  if (kDyn) {
+    T = p.lens[0];
+    start_pos = p.lens[1];
+    if (!lengths_ok(T, start_pos, p.T, p.kv_capacity, p.ring_rows, p.window)) {
+      if (blockIdx.x == 0 && threadIdx.x == 0) atomicOr(p.err, kErrLengths);
+      return;
+    }
+    tiles_per_head = (int)((T + p.tok_per_tile - 1) / p.tok_per_tile);
+    if ((int)(blockIdx.x >> 1) >= tiles_per_head * p.Hkv) return;  // nothing set up yet
+  }
+
   // work unit: (d-half, kv head, query tile); latest tokens first
   const int dh = blockIdx.x & 1;
   const int rest = blockIdx.x >> 1;
   const int kh = rest % p.Hkv;
-  const int tile = p.tiles_per_head - 1 - rest / p.Hkv;
+  const int tile = tiles_per_head - 1 - rest / p.Hkv;
   const int64_t t0 = (int64_t)tile * p.tok_per_tile;
-  const int64_t t_end = min(t0 + p.tok_per_tile, p.T);
-  const int64_t pos_first = p.start_pos + t0;
-  const int64_t pos_last = p.start_pos + t0 + p.tok_per_tile - 1;
+  const int64_t t_end = min(t0 + p.tok_per_tile, T);
+  const int64_t pos_first = start_pos + t0;
+  const int64_t pos_last = start_pos + t0 + p.tok_per_tile - 1;
   const int64_t kmin = p.window > 0 ? max((int64_t)0, pos_first - p.window + 1) : 0;
   const int64_t kt_first = kmin / kBN;
-  const int n = (int)((p.start_pos + t_end - 1) / kBN - kt_first + 1);
+  const int n = (int)((start_pos + t_end - 1) / kBN - kt_first + 1);
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < kNumBars; ++i)
@@ -239,8 +256,8 @@ bf16_d512_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
     const int tok = row / p.group;
     const bool row_exists = tok < p.tok_per_tile;
     const int64_t t = t0 + tok;
-    const bool row_valid = row_exists && t < p.T;
-    const int64_t pos = p.start_pos + t;
+    const bool row_valid = row_exists && t < T;
+    const int64_t pos = start_pos + t;
     const int h = kh * p.group + row % p.group;
     const uint32_t lane_off = (uint32_t)(warp * 32) << 16;
     const uint32_t tO = tmem + lane_off + kColO;
@@ -382,11 +399,16 @@ int launch_bf16_d512(const Call& c) {
   static int attr_done[64] = {0};
   if (c.device < 0 || c.device >= 64) return kErrDevice;
   if (!attr_done[c.device]) {
-    if (cudaFuncSetAttribute(bf16_d512_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             kSmemAlloc) != cudaSuccess ||
-        cudaFuncSetAttribute(bf16_d512_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             kSmemAlloc) != cudaSuccess)
-      return kErrLaunch;
+    const void* fns[4] = {(const void*)bf16_d512_kernel<true, false>,
+                          (const void*)bf16_d512_kernel<false, false>,
+                          (const void*)bf16_d512_kernel<true, true>,
+                          (const void*)bf16_d512_kernel<false, true>};
+    for (const void* fn : fns)
+      if (cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemAlloc) !=
+          cudaSuccess) {
+        cudaGetLastError();
+        return kErrLaunch;
+      }
     attr_done[c.device] = 1;
   }
   const int group = c.H / c.Hkv;
@@ -416,6 +438,8 @@ int launch_bf16_d512(const Call& c) {
   p.ring_rows = ring_rows(c);
   p.T = c.T;
   p.start_pos = c.start_pos;
+  p.lens = c.lens;
+  p.kv_capacity = c.max_seq_len;
   p.H = c.H;
   p.Hkv = c.Hkv;
   p.group = group;
@@ -427,10 +451,17 @@ int launch_bf16_d512(const Call& c) {
   p.wait_limit_ns = c.wait_limit_ns;
   p.flags = c.flags;
   const dim3 grid((unsigned)(2 * tiles * c.Hkv));
-  if (p.scale_log2 > 0.f)
-    bf16_d512_kernel<true><<<grid, kThreads, kSmemAlloc, c.stream>>>(tq, tk, tv, p);
-  else
-    bf16_d512_kernel<false><<<grid, kThreads, kSmemAlloc, c.stream>>>(tq, tk, tv, p);
+  const bool fold = p.scale_log2 > 0.f;
+  if (c.lens) {
+    if (fold)
+      bf16_d512_kernel<true, true><<<grid, kThreads, kSmemAlloc, c.stream>>>(tq, tk, tv, p);
+    else
+      bf16_d512_kernel<false, true><<<grid, kThreads, kSmemAlloc, c.stream>>>(tq, tk, tv, p);
+  } else if (fold) {
+    bf16_d512_kernel<true, false><<<grid, kThreads, kSmemAlloc, c.stream>>>(tq, tk, tv, p);
+  } else {
+    bf16_d512_kernel<false, false><<<grid, kThreads, kSmemAlloc, c.stream>>>(tq, tk, tv, p);
+  }
   return cudaGetLastError() == cudaSuccess ? kOk : kErrLaunch;
 }
 

@@ -37,7 +37,10 @@ struct F32Params {
   int64_t q_stride;        // elements from one token's q / out row to the next
   int64_t kv_head_stride;  // elements from one kv head's cache block to the next
   int64_t ring_rows;       // > 0: key j is in cache row j % ring_rows; 0: in row j
-  int64_t T, start_pos, L;
+  int64_t T, start_pos, L;  // graph entry: T = the largest T, start_pos unused
+  const int64_t* lens;      // graph entry: device {T, start_pos}; else null
+  int64_t kv_capacity;      // rows per kv head in the cache
+  unsigned* err;            // device error word
   int H, Hkv, group, D, window;
   float scale_log2;        // scale * log2(e)
   int64_t rows_per_head;   // T * group
@@ -66,21 +69,34 @@ f32_attention_kernel(const F32Params p) {
   float* sQ = sV + kKeysPerTile * D;           // [8][D]
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  // Chunk length and position: kernel parameters, or (graph entry) read from
+  // device memory at run time, with the grid sized for the largest T.
+  int64_t start_pos = p.start_pos, rows_per_head = p.rows_per_head;
+  if (p.lens) {
+    const int64_t T = p.lens[0];
+    start_pos = p.lens[1];
+    if (!lengths_ok(T, start_pos, p.T, p.kv_capacity, p.ring_rows, p.window)) {
+      if (blockIdx.x == 0 && blockIdx.y == 0 && threadIdx.x == 0) atomicOr(p.err, kErrLengths);
+      return;
+    }
+    rows_per_head = T * p.group;
+  }
   const int kh = blockIdx.y;
   const int64_t r0 = (int64_t)blockIdx.x * kRowsPerBlock;
+  if (r0 >= rows_per_head) return;  // the whole block (graph entry, shorter chunk)
   const int64_t r = r0 + warp;
-  const bool active = r < p.rows_per_head;
+  const bool active = r < rows_per_head;
   const int64_t t = active ? r / p.group : 0;
   const int h = kh * p.group + (active ? (int)(r % p.group) : 0);
-  const int64_t pos = p.start_pos + t;
+  const int64_t pos = start_pos + t;
 
   for (int d = lane; d < D; d += 32)
     sQ[warp * D + d] = active ? p.q[t * p.q_stride + h * (int64_t)D + d] : 0.f;
 
   // Keys any row of this block can see.
-  const int64_t r_last = min(r0 + kRowsPerBlock, p.rows_per_head) - 1;
-  const int64_t pos_lo = p.start_pos + r0 / p.group;
-  const int64_t pos_hi = p.start_pos + r_last / p.group;
+  const int64_t r_last = min(r0 + kRowsPerBlock, rows_per_head) - 1;
+  const int64_t pos_lo = start_pos + r0 / p.group;
+  const int64_t pos_hi = start_pos + r_last / p.group;
   const int64_t kmin = p.window > 0 ? max((int64_t)0, pos_lo - p.window + 1) : 0;
   const int64_t kmax = pos_hi;
 
@@ -199,6 +215,9 @@ int launch_f32(const Call& c) {
   p.q_stride = c.qkv_dim;
   p.kv_head_stride = c.max_seq_len * (int64_t)c.D;
   p.ring_rows = ring_rows(c);
+  p.lens = c.lens;
+  p.kv_capacity = c.max_seq_len;
+  p.err = c.err;
   p.T = c.T;
   p.start_pos = c.start_pos;
   p.L = c.start_pos + c.T;

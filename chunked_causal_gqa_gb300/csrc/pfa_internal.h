@@ -28,18 +28,24 @@ struct Call {
   int64_t qkv_dim;        // elements from one token's q / out row to the next (>= H*D)
   int64_t max_seq_len;    // rows per kv head in k / v (kv head stride = max_seq_len * D)
   int ring;               // 1: key j lives in row j % max_seq_len (circular cache)
+  // Graph entry: device pointer to {T, start_pos}, read by the kernels at run
+  // time; T above is then the largest T (the grid is sized for it).  Null
+  // for every other entry point.
+  const int64_t* lens;
 };
 
 // Rows at the start of each kv head's block that hold written keys: L for a
 // linear cache, min(L, capacity) for a circular one.  Rows past them are
 // never read (TMA reads them as zeros).
 inline int64_t cache_rows_written(const Call& c) {
+  if (c.lens) return c.max_seq_len;  // unknown on the host: the whole allocation
   const int64_t L = c.start_pos + c.T;
   return (c.ring && c.max_seq_len < L) ? c.max_seq_len : L;
 }
 // Modulus of the key -> cache row map once a circular cache has wrapped
 // (L > capacity); 0 means key j is in row j.
 inline int ring_rows(const Call& c) {
+  if (c.lens) return c.ring ? (int)c.max_seq_len : 0;  // j % capacity == j before a wrap
   return (c.ring && c.max_seq_len < c.start_pos + c.T) ? (int)c.max_seq_len : 0;
 }
 

@@ -47,6 +47,18 @@ __device__ __forceinline__ uint64_t globaltimer_ns() {
 
 // Error bits recorded in the device error word.
 constexpr unsigned kErrTimeout = 1u;
+constexpr unsigned kErrLengths = 2u;  // device-side {T, start_pos} failed its checks
+
+// Graph entry: checks the run-time {T, start_pos} against the capacities the
+// grid and the tensor maps were built for.
+__device__ __forceinline__ bool lengths_ok(int64_t T, int64_t sp, int64_t max_T, int64_t cap,
+                                           int64_t ring_rows, int window) {
+  if (T < 0 || T > max_T || sp < 0 || sp + T > ((int64_t)1 << 31) - 4096) return false;
+  if (ring_rows == 0) return sp + T <= cap;
+  const int64_t span = (int64_t)window + T - 1 < sp + T ? (int64_t)window + T - 1 : sp + T;
+  return cap >= span;
+}
+
 
 // Bounded wait for the completion of the phase with parity `parity`.
 // Returns true on completion.  Returns false (without completing) when the

@@ -61,8 +61,11 @@ typedef enum {
                                 by pfa_last_device_error)                           */
     PFA_ERR_VALUE = -8,      /* scale is not a finite number                        */
     PFA_ERR_ALIAS = -9,      /* out overlaps q, k_cache or v_cache                  */
-    PFA_ERR_SCRATCH = -10    /* the shape needs more scratch than
+    PFA_ERR_SCRATCH = -10,   /* the shape needs more scratch than
                                 pfa_prefill_attention_noalloc holds                 */
+    PFA_ERR_LENGTHS = -11    /* pfa_prefill_attention_graph: the {T, start_pos} read
+                                on the device did not fit its capacities (reported
+                                after a sync by pfa_last_device_error)              */
 } pfa_status;
 
 /*
@@ -195,6 +198,49 @@ PFA_API int pfa_workspace_bytes(int64_t T, int64_t start_pos, int num_heads, int
                                 int head_dim, int window, int dtype, size_t *bytes);
 
 /*
+ * pfa_prefill_attention_graph -- pfa_prefill_attention_cache with the chunk's
+ * length and position read from device memory when the kernel runs, so that
+ * one captured CUDA graph replays for any chunk: the launch's parameters and
+ * grid depend only on capacities.  This is the graph-replay requirement of
+ * the TensorSharp2 Gemma-4 prefill design (section 4, R5: inputs refreshed
+ * in place, the same pointers and shapes every chunk; section 6, Phase 2) and
+ * of the FreeToken draft-graph change ("replay holds at any sequence length":
+ * the lengths live in fixed device buffers written before each replay).
+ *
+ *   lengths  device pointer (8-byte aligned) to two int64: {T, start_pos} of
+ *            the chunk, read by the kernel at run time (write them on the
+ *            stream, or before it, ahead of each launch or replay).
+ *   max_T    the largest T: q and out hold max_T rows of qkv_dim elements;
+ *            the grid is sized for it (CTAs beyond the run-time chunk exit at
+ *            once).  1 <= max_T <= max_seq_len (max_T == 0 is a no-op).
+ *   q, k_cache, v_cache, out, num_heads .. dtype, qkv_dim, max_seq_len, ring
+ *            as for pfa_prefill_attention_cache; for PFA_BF16 a ring's
+ *            max_seq_len must be a multiple of 128.
+ *
+ * Run-time checks: 0 <= T <= max_T, start_pos >= 0, and L = start_pos + T <=
+ * max_seq_len (linear) or max_seq_len >= min(L, window + T - 1) (ring).  A
+ * launch whose lengths fail them writes nothing and records PFA_ERR_LENGTHS,
+ * which pfa_last_device_error returns.  T == 0 writes nothing.
+ *
+ * Cache rows past L: the host cannot clip the tensor maps at a run-time L, so
+ * for PFA_BF16 the rows of the last 128-key tile (64 for head_dim 512) past
+ * L are read and weighted by exactly zero -- they must hold finite values
+ * (never-written rows of a zero-initialised cache do).  The fp32 path reads
+ * no row past L.
+ *
+ * Always the plain schedule (no workspace).  Capture: the first call of the
+ * library on a device does per-device set-up (device queries, a memset of
+ * the device error word, kernel attributes) that must not happen inside a
+ * stream capture; make one call of any entry point on the device first.
+ * Other behaviour, ownership and errors: as for pfa_prefill_attention_cache.
+ */
+PFA_API int pfa_prefill_attention_graph(const void *q, const void *k_cache, const void *v_cache,
+                                        void *out, const int64_t *lengths, int64_t max_T,
+                                        int num_heads, int num_kv_heads, int head_dim, int window,
+                                        float scale, int dtype, int64_t qkv_dim,
+                                        int64_t max_seq_len, int ring, void *stream);
+
+/*
  * pfa_schedule -- which schedule pfa_prefill_attention_ws runs for this shape
  * on the current device when its workspace is at least *workspace_bytes
  * (the value pfa_workspace_bytes reports):
@@ -261,8 +307,10 @@ PFA_API const char *pfa_status_string(int status);
 
 /*
  * pfa_last_device_error -- synchronise `stream`, then return and clear the
- * device-side error word of the current device: PFA_OK, or PFA_ERR_TIMEOUT if
- * a kernel launched since the last call gave up on a wait.  Returns
+ * device-side error word of the current device: PFA_OK, PFA_ERR_TIMEOUT if
+ * a kernel launched since the last call gave up on a wait, or
+ * PFA_ERR_LENGTHS if a pfa_prefill_attention_graph launch found its
+ * run-time lengths out of range (timeouts take precedence).  Returns
  * PFA_ERR_DEVICE if the stream cannot be synchronised (the CUDA error is then
  * the runtime's).
  */

@@ -101,3 +101,32 @@ def test_python_binding_checks_tensors():
         pkg.prefill_attention(q, k[:, :3], k[:, :3])
     with pytest.raises(ValueError):
         pkg.prefill_attention(q[0], k, k)
+
+
+def cache_call(lib, q=A, k=B, v=C, o=O, T=16, sp=100, H=8, Hkv=2, D=128, w=64, dt=BF16,
+               qkv_dim=None, cap=512, ring=1):
+    qkv_dim = H * D if qkv_dim is None else qkv_dim
+    return lib.pfa_prefill_attention_cache(q, k, v, o, T, sp, H, Hkv, D, w, 0.1, dt, qkv_dim,
+                                           cap, ring, None, 0, None)
+
+
+def test_cache_layout_validation_without_gpu(lib):
+    assert cache_call(lib, ring=1, w=0) == -2              # ring needs a window
+    assert cache_call(lib, sp=1000, w=600) == -2           # 600 + 15 rows > 512
+    assert cache_call(lib, sp=1000, cap=300, w=100) == -2  # wrapped bf16 ring, 300 % 128
+    assert cache_call(lib, ring=0, cap=100) == -2          # linear cache shorter than L
+    assert cache_call(lib, qkv_dim=8 * 128 - 8) == -2      # rows shorter than the heads
+    assert cache_call(lib, qkv_dim=8 * 128 + 4) == -4      # 2056-byte rows
+    assert cache_call(lib, T=0, q=None, k=None, v=None, o=None) == 0
+
+
+def test_graph_entry_validation_without_gpu(lib):
+    def g(lens=0x80000, max_T=16, cap=512, ring=0, w=0, dt=BF16, D=128):
+        return lib.pfa_prefill_attention_graph(A, B, C, O, lens, max_T, 8, 2, D, w, 0.1, dt,
+                                               8 * D, cap, ring, None)
+    assert g(lens=None) == -1
+    assert g(lens=0x80004) == -4                           # lengths not 8-byte aligned
+    assert g(max_T=-1) == -2
+    assert g(max_T=600) == -2                              # max_T > max_seq_len
+    assert g(ring=1, w=0) == -2
+    assert g(max_T=0) == 0                                 # no-op
