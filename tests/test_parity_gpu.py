@@ -271,3 +271,35 @@ def test_errors_from_the_device_path():
     k = torch.zeros(2, 4, 128, dtype=torch.bfloat16, device=d)
     empty = pkg.prefill_attention(q[:0], k[:, :0], k[:, :0])
     assert empty.shape == (0, 8, 128)
+
+
+# Score profiles over the four 128-key tiles of a 500-key cache, in units of
+# the shared component's score (~16 in log2 units): exercise every exponent-
+# base path of the bf16 softmax -- a first tile far below 0, a first tile far
+# above 0, a maximum that jumps by more than 2^8 in a later tile, and a plain
+# profile.
+SCORE_PROFILES = {
+    "first_tile_far_below": (-6.0, 0.0, 1.5, 0.2),
+    "first_tile_far_above": (2.0, 0.0, -1.0, 0.5),
+    "late_jump": (0.1, 0.2, 1.5, 3.0),
+    "flat": (0.0, 0.0, 0.0, 0.0),
+}
+
+
+@pytest.mark.parametrize("D", [128, 512])
+@pytest.mark.parametrize("profile", sorted(SCORE_PROFILES))
+def test_softmax_dynamic_range(profile, D):
+    H, Hkv, T, sp = 8, 2, 200, 300
+    L = sp + T
+    g = torch.Generator().manual_seed(17)
+    u = torch.randn(D, generator=g)
+    q = (u + 0.1 * torch.randn(T, H, D, generator=g)).to(torch.bfloat16)
+    beta = torch.empty(L)
+    for tile, b in enumerate(SCORE_PROFILES[profile]):
+        beta[tile * 128:(tile + 1) * 128] = b
+    k = (beta[None, :, None] * u[None, None, :] + 0.3 * torch.randn(Hkv, L, D, generator=g))
+    k = k.to(torch.bfloat16)
+    v = torch.randn(Hkv, L, D, generator=g).to(torch.bfloat16)
+    got = G.to_np(G.run(q, k, v))
+    want = oracle.prefill_attention(q, k, v)
+    G.check(got, want, "bf16", f"{profile} D{D}")
