@@ -39,6 +39,7 @@ if ROOT not in sys.path:
 METRIC = "prefill-attention TFLOP/s (causal) & prompt-tok/s per layer; % of bf16 peak"
 KERNEL_SOURCES = {
     "bf16_d128": "chunked_causal_gqa_gb300/csrc/pfa_bf16_d128.cu",
+    "bf16_d512": "chunked_causal_gqa_gb300/csrc/pfa_bf16_d512.cu",
     "f32": "chunked_causal_gqa_gb300/csrc/pfa_f32.cu",
 }
 
