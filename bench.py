@@ -41,7 +41,12 @@ KERNEL_SOURCES = {
     "bf16_d128": "chunked_causal_gqa_gb300/csrc/pfa_bf16_d128.cu",
     "bf16_d512": "chunked_causal_gqa_gb300/csrc/pfa_bf16_d512.cu",
     "f32": "chunked_causal_gqa_gb300/csrc/pfa_f32.cu",
+    "tf32x3_d128": "chunked_causal_gqa_gb300/csrc/pfa_tf32_d128.cu",
 }
+
+# Nominal dense tf32 / bf16 tensor rates of the part (1.1 and 2.25 PFLOP/s):
+# the tf32 peak is the measured bf16 peak times this ratio.
+TF32_OVER_BF16 = 1.1 / 2.25
 
 
 def dist_env():
@@ -52,7 +57,9 @@ def dist_env():
 
 
 def kernel_name(wl) -> str:
-    return "f32" if wl.dtype == "f32" else f"bf16_d{wl.head_dim}"
+    if wl.dtype == "f32":
+        return "tf32x3_d128" if wl.head_dim == 128 else "f32"
+    return f"bf16_d{wl.head_dim}"
 
 
 def source_hash(name: str) -> str:
@@ -329,8 +336,17 @@ def run_ours(args, wl):
 
     peaks, peak_src = measured_peaks()
     kname = kernel_name(wl)
-    if wl.dtype == "f32":
-        # fp32 SIMT path: bound by the fp32 FMA pipe
+    extra = {}
+    if kname == "tf32x3_d128":
+        # fp32 head_dim 128: three tf32 products per contraction on the tensor
+        # cores; `achieved` counts the attention's own flops, the tensor pipe
+        # executes three times as many
+        peak = float(peaks["bf16_tflops"]) * TF32_OVER_BF16
+        bound = "tensor"
+        peak_note = f"tf32 = bf16_tflops ({peak_src}, burst) x nominal tf32/bf16 1.1/2.25"
+        extra = {"tensor_flops_per_flop": 3}
+    elif wl.dtype == "f32":
+        # fp32 CUDA-core path: bound by the fp32 FMA pipe
         peak = 2.0 * 128 * 152 * (peaks.get("sm_max_mhz", 2070.0) * 1e6) / 1e12
         bound, peak_note = "alu", "fp32 FMA: 128 lanes x 2 flops x 152 SMs x max SM clock"
     else:
@@ -342,7 +358,7 @@ def run_ours(args, wl):
                 "kernel": kname, "peak_source": peak_note,
                 "timed_span": ("one step: main kernel + merge kernel" if ws_bytes > 0
                                else "one step: one kernel launch"),
-                "algorithmic_bytes": wl.algorithmic_bytes()}
+                "algorithmic_bytes": wl.algorithmic_bytes(), **extra}
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:

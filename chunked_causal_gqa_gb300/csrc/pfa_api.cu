@@ -343,7 +343,7 @@ int attach_workspace(Call* c, int dtype, void* workspace, size_t workspace_bytes
 int dispatch(const Call& c, int dtype) {
   int rc;
   if (dtype == PFA_F32)
-    rc = launch_f32(c);
+    rc = c.D == 128 ? launch_tf32_d128(c) : launch_f32(c);
   else if (c.D == 128)
     rc = launch_bf16_d128(c);
   else

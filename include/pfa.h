@@ -323,8 +323,9 @@ PFA_API int pfa_version(void);
  * pfa_debug_configure -- test hook for the device-side wait limits.
  *   wait_limit_ms  time limit of every device-side wait in later launches
  *                  (<= 0 restores the default of 2000 ms).
- *   force_timeout  non-zero makes the next bf16 launches wait once on a
- *                  barrier that nothing signals, so the limit expires and the
+ *   force_timeout  non-zero makes the next tensor-core launches (bf16, and
+ *                  fp32 with head_dim 128) wait once on a barrier that
+ *                  nothing signals, so the limit expires and the
  *                  kernel takes its early-exit path (PFA_ERR_TIMEOUT);
  *                  zero restores normal operation.
  * Process-wide setting; not thread-safe with concurrent launches.

@@ -59,6 +59,17 @@ F32_CASES = [
     (8, 2, 512, 33, 20, 0),
     (6, 3, 36, 40, 0, 5),
     (2, 2, 128, 1, 100, 0),
+    # head_dim 128: the 3xTF32 tensor-core kernel (key tiles of 64)
+    (8, 2, 128, 300, 200, 0),      # GQA 4, ragged T and L
+    (8, 2, 128, 129, 0, 0),        # one token past a tile, prompt from 0
+    (4, 4, 128, 130, 5, 0),        # group 1: 128 tokens per tile
+    (16, 2, 128, 100, 50, 0),      # group 8
+    (6, 2, 128, 150, 20, 0),       # group 3: 126-row tiles
+    (128, 1, 128, 5, 3, 0),        # group 128: 1 token per tile
+    (8, 2, 128, 300, 500, 100),    # window inside one key tile
+    (8, 2, 128, 300, 500, 65),     # window band crossing key tiles
+    (8, 2, 128, 64, 3000, 0),      # short chunk deep in the cache
+    (32, 8, 128, 200, 1000, 0),    # Mistral-like heads
 ]
 
 
@@ -103,6 +114,18 @@ def test_long_chunk_sampled_parity(name, workspace):
     got = G.to_np(out)[[t for t, _ in rows], [h for _, h in rows]]
     G.check(got, want, "bf16", name)
     assert torch.isfinite(out.float()).all()
+
+
+def test_f32_long_chunk_sampled_parity_and_bits():
+    """The 3xTF32 path at a size where it streams 16k keys per query tile."""
+    wl = W.WORKLOADS["f32_chunk_16k"]
+    q, k, v = W.make_inputs(wl)
+    out = G.run(q, k, v, window=wl.window, scale=wl.scale)
+    rows = G.sample_rows(wl.T, wl.num_heads, 24, seed=wl.seeds[0])
+    want = oracle.prefill_attention_rows(q, k, v, rows, window=wl.window, scale=wl.scale)
+    got = G.to_np(out)[[t for t, _ in rows], [h for _, h in rows]]
+    G.check(got, want, "f32", wl.name)
+    assert G.digest(G.run(q, k, v, window=wl.window, scale=wl.scale)) == G.digest(out)
 
 
 def test_gemma_window_layer_full_parity():

@@ -12,9 +12,9 @@ from tests import gpu_util as G
 pytestmark = pytest.mark.gpu
 
 
-@pytest.mark.parametrize("D", [128, 512])
-def test_forced_wait_timeout_is_reported_and_context_survives(D):
-    q, k, v = W.make_random(100, 40, 8, 2, D, "bf16", seed=51)
+@pytest.mark.parametrize("D,dtype", [(128, "bf16"), (512, "bf16"), (128, "f32")])
+def test_forced_wait_timeout_is_reported_and_context_survives(D, dtype):
+    q, k, v = W.make_random(100, 40, 8, 2, D, dtype, seed=51)
     d = G.dev()
     qd, kd, vd = q.to(d), k.to(d), v.to(d)
     pkg.debug_configure(wait_limit_ms=50.0, force_timeout=True)
@@ -26,4 +26,4 @@ def test_forced_wait_timeout_is_reported_and_context_survives(D):
     assert status == -7, pkg.status_string(status)
     assert pkg.last_device_error() == 0          # the word was cleared
     got = G.to_np(G.run(q, k, v))                # the context still works
-    G.check(got, oracle.prefill_attention(q, k, v), "bf16", "after timeout")
+    G.check(got, oracle.prefill_attention(q, k, v), dtype, "after timeout")
