@@ -15,22 +15,25 @@
 // dimensions) and each accumulates its half of P V: 1.5x the minimum tensor
 // work, in exchange for fitting S and O in tensor memory.
 //
-// Warp roles (7 warps):
+// Key tiles of 128: every QK^T product is M=128 N=128 K=16, so the query tile
+// (read from shared memory by every product) is read once per 128 keys.  K
+// (128 keys x 512) does not fit beside Q, so it streams through a ring of
+// 16 KB slots as eight 64-column chunks; this CTA's half of V streams as two
+// 64-key chunks of 32 KB (two slots each).  The producer fills the ring in
+// the order the MMA warp consumes it: K(0), K(1), V(0), K(2), V(1), ...
+//
+// Warp roles (6 warps):
 //   warps 0-3  softmax and epilogue (TMEM lanes 0-127, one row per thread)
-//   warp  4    TMA producer: Q once, then per key tile K (64 keys x 512) as
-//              eight 64-column chunks, each with its own slot and barriers
+//   warp  4    TMA producer: Q once, then the K and V chunks
 //   warp  5    TMEM allocator and MMA issuer (the whole warp runs the loop;
 //              one elected lane issues each group of tcgen05.mma)
-//   warp  6    TMA producer: this CTA's half of V (64 keys x 256)
-// Q takes 128 KB of shared memory, so K and V have one tile slot each; K's
-// chunks are refilled one by one as the products reading them complete.
 //
-// Tensor memory: [0,64) S_0, [64,128) S_1 (double-buffered scores; after the
-// softmax the first 32 columns hold P as packed bf16 pairs), [256,512) O half.
+// Tensor memory: [0,128) S_0, [128,256) S_1 (double-buffered scores; after the
+// softmax the first 64 columns hold P as packed bf16 pairs), [256,512) O half.
 //
 // MMA issue order: S(0), S(1), O += P(0) V(0), S(2), O += P(1) V(1), ...
 // The softmax of tile i overlaps S(i+1); it waits for O += P(i-1) V(i-1)
-// (barrier kBarO, one phase per product) before it may rescale O.
+// (barrier kBarO, one phase per tile) before it may rescale O.
 #include "pfa_internal.h"
 #include "pfa_ptx.cuh"
 
@@ -42,26 +45,28 @@ namespace pfa {
 namespace {
 
 constexpr int kBM = 128;                  // query rows per tile
-constexpr int kBN = 64;                   // keys per K/V tile
+constexpr int kBN = 128;                  // keys per tile
+constexpr int kVKeys = 64;                // keys per V chunk
 constexpr int kDHalf = 256;               // output columns per CTA
 constexpr int kQChunk = 128 * 128;        // 128 rows x 64 bf16 (one 128-byte swizzle span)
-constexpr int kKChunk = kBN * 128;        // 64 keys x 64 bf16
+constexpr int kSlot = 16384;              // ring slot: a K chunk, or half a V chunk
+constexpr int kRing = 6;                  // ring slots
+constexpr int kVSub = kVKeys * 128;       // 64 keys x 64 bf16 of V (8 KB)
 constexpr int kSmemQ = 0;                 // 8 chunks: 128 KB
-constexpr int kSmemK = 8 * kQChunk;       // 8 chunks: 64 KB
-constexpr int kSmemV = kSmemK + 8 * kKChunk;   // 4 chunks: 32 KB
-constexpr int kSmemBars = kSmemV + 4 * kKChunk;  // 229376
+constexpr int kSmemRing = 8 * kQChunk;    // 6 slots: 96 KB
+constexpr int kSmemBars = kSmemRing + kRing * kSlot;  // 229376
 constexpr int kSmemAlloc = kSmemBars + 256 + 1024;
-constexpr int kThreads = 224;
+constexpr int kThreads = 192;
 constexpr float kRescaleThreshold = 8.0f;
 
-constexpr int kBarQ = 0, kBarVFull = 1, kBarVEmpty = 2;
-constexpr int kBarS = 3;        // 2
-constexpr int kBarP = 5;        // 2
-constexpr int kBarO = 7;        // one phase per P V product
-constexpr int kBarDrain = 8;
-constexpr int kBarKFull = 9;    // 8: one per 64-column chunk of the K tile
-constexpr int kBarKEmpty = 17;  // 8
-constexpr int kNumBars = 25;
+constexpr int kBarQ = 0;
+constexpr int kBarS = 1;                  // 2
+constexpr int kBarP = 3;                  // 2
+constexpr int kBarO = 5;                  // one phase per tile's P V
+constexpr int kBarDrain = 6;
+constexpr int kBarFull = 7;               // kRing
+constexpr int kBarEmpty = kBarFull + kRing;  // kRing
+constexpr int kNumBars = kBarEmpty + kRing;
 static_assert(kNumBars * 8 + 8 <= 256, "barrier area");
 constexpr int kOffTmemSlot = kNumBars * 8;
 constexpr int kOffAbort = kOffTmemSlot + 4;
@@ -127,6 +132,9 @@ bf16_d512_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
   const int64_t kmin = p.window > 0 ? max((int64_t)0, pos_first - p.window + 1) : 0;
   const int64_t kt_first = kmin / kBN;
   const int n = (int)((start_pos + t_end - 1) / kBN - kt_first + 1);
+  auto key_row = [&](int64_t key) -> int {
+    return (int)(p.ring_rows > 0 ? key % p.ring_rows : key);
+  };
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < kNumBars; ++i)
@@ -143,65 +151,66 @@ bf16_d512_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
 
-  if (warp == 4 || warp == 6) {
-    // ------------------------------------------------------------ producers
-    // warp 4 loads Q once and then K tiles; warp 6 loads this CTA's V halves.
-    // Separate threads keep a K load from queueing behind the V buffer.
+  // Ring order (producer and consumer): for i = 0..n-1: the eight K chunks of
+  // tile i, then (i >= 1) the V chunks of tile i-1; after the last tile, the V
+  // chunks of tile n-1.  A V chunk is two consecutive slot loads; with eight
+  // K loads per tile its pair always starts on an even slot of the 6-slot
+  // ring, so its 32 KB are contiguous.
+
+  if (warp == 4) {
+    // ------------------------------------------------------------ producer
     if (lane == 0) {
-      const bool is_k = (warp == 4);
-      const CUtensorMap* map = is_k ? &tm_k : &tm_v;
-      tma_prefetch_desc(map);
-      if (is_k) {
-        tma_prefetch_desc(&tm_q);
-        const int hq = kh * p.group;
-        mbar_arrive_expect_tx(bar(kBarQ), 8u * 128u * (uint32_t)(p.group * p.tok_per_tile));
-        for (int c = 0; c < 8; ++c)
-          tma_load_3d(sbase + kSmemQ + c * kQChunk, &tm_q, bar(kBarQ), 64 * c, hq, (int)t0);
-      }
-      if (is_k) {
-        // K: each 64-column chunk has its own slot and barriers, so chunk c of
-        // the next tile loads as soon as the products that read chunk c of
-        // this tile are done.
-        int issued = 0;  // tiles whose 8 chunks were all issued
-        int part = 0;    // chunks issued of the tile after those
-        bool ok = true;
-        for (int i = 0; i < n && ok; ++i) {
-          const int key0 = (int)((kt_first + i) * kBN);
-          for (int c = 0; c < 8; ++c) {
-            if (!(ok = mbar_wait(bar(kBarKEmpty + c), (uint32_t)(i & 1) ^ 1u, abort_flag, p.err,
-                                 lim)))
-              break;
-            mbar_arrive_expect_tx(bar(kBarKFull + c), (uint32_t)kKChunk);
-            tma_load_3d(sbase + kSmemK + c * kKChunk, map, bar(kBarKFull + c), 64 * c,
-                        p.ring_rows > 0 ? key0 % p.ring_rows : key0, kh);
-            ++part;
-          }
-          if (ok) {
-            ++issued;
-            part = 0;
-          }
-        }
-        // no copy may be in flight when the CTA exits
-        mbar_wait(bar(kBarQ), 0, abort_flag, p.err, lim, true);
+      tma_prefetch_desc(&tm_q);
+      tma_prefetch_desc(&tm_k);
+      tma_prefetch_desc(&tm_v);
+      const int hq = kh * p.group;
+      mbar_arrive_expect_tx(bar(kBarQ), 8u * 128u * (uint32_t)(p.group * p.tok_per_tile));
+      for (int c = 0; c < 8; ++c)
+        tma_load_3d(sbase + kSmemQ + c * kQChunk, &tm_q, bar(kBarQ), 64 * c, hq, (int)t0);
+      uint32_t li = 0;  // slot loads issued
+      bool ok = true;
+      auto slot_wait = [&](uint32_t* dst) -> bool {
+        const uint32_t s = li % kRing, ph = (li / kRing) & 1u;
+        if (!mbar_wait(bar(kBarEmpty + s), ph ^ 1u, abort_flag, p.err, lim)) return false;
+        mbar_arrive_expect_tx(bar(kBarFull + s), (uint32_t)kSlot);
+        *dst = s;
+        return true;
+      };
+      auto load_k = [&](int i) -> bool {
+        const int row = key_row((kt_first + i) * kBN);
         for (int c = 0; c < 8; ++c) {
-          const int loads = issued + (c < part ? 1 : 0);  // loads issued into chunk c
-          if (loads > 0)
-            mbar_wait(bar(kBarKFull + c), (uint32_t)(loads - 1) & 1u, abort_flag, p.err, lim, true);
+          uint32_t s;
+          if (!slot_wait(&s)) return false;
+          tma_load_3d(sbase + kSmemRing + s * kSlot, &tm_k, bar(kBarFull + s), 64 * c, row, kh);
+          ++li;
         }
-      } else {
-        int issued = 0;
-        for (int i = 0; i < n; ++i) {
-          const int key0 = (int)((kt_first + i) * kBN);
-          if (!mbar_wait(bar(kBarVEmpty), (uint32_t)(i & 1) ^ 1u, abort_flag, p.err, lim)) break;
-          mbar_arrive_expect_tx(bar(kBarVFull), (uint32_t)(4 * kKChunk));
-          for (int c = 0; c < 4; ++c)
-            tma_load_3d(sbase + kSmemV + c * kKChunk, map, bar(kBarVFull), dh * kDHalf + 64 * c,
-                        p.ring_rows > 0 ? key0 % p.ring_rows : key0, kh);
-          ++issued;
+        return true;
+      };
+      auto load_v = [&](int i) -> bool {
+        for (int h = 0; h < 2; ++h) {
+          const int row = key_row((kt_first + i) * kBN + h * kVKeys);
+          for (int part = 0; part < 2; ++part) {
+            uint32_t s;
+            if (!slot_wait(&s)) return false;
+            for (int b = 0; b < 2; ++b)
+              tma_load_3d(sbase + kSmemRing + s * kSlot + b * kVSub, &tm_v, bar(kBarFull + s),
+                          dh * kDHalf + 64 * (2 * part + b), row, kh);
+            ++li;
+          }
         }
-        if (issued > 0)
-          mbar_wait(bar(kBarVFull), (uint32_t)(issued - 1) & 1u, abort_flag, p.err, lim, true);
+        return true;
+      };
+      for (int i = 0; i < n && ok; ++i) {
+        ok = load_k(i);
+        if (ok && i > 0) ok = load_v(i - 1);
       }
+      if (ok) ok = load_v(n - 1);
+      // No copy may be in flight when the CTA exits.  On the normal path the
+      // MMA warp has already consumed every load, so these return at once.
+      mbar_wait(bar(kBarQ), 0, abort_flag, p.err, lim, true);
+      const uint32_t first = li > (uint32_t)kRing ? li - kRing : 0;
+      for (uint32_t j = first; j < li; ++j)
+        mbar_wait(bar(kBarFull + j % kRing), (j / kRing) & 1u, abort_flag, p.err, lim, true);
     }
   } else if (warp == 5) {
     // ------------------------------------------------------------ MMA issuer
@@ -212,18 +221,31 @@ bf16_d512_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
       bool ok = mbar_wait_warp(bar(kBarQ), 0, abort_flag, p.err, lim);
       tc_fence_after();
       bool issued = false;
+      uint32_t li = 0;  // slot loads consumed
+      auto slot_ready = [&](uint32_t* s) -> bool {
+        *s = li % kRing;
+        if (!mbar_wait_warp(bar(kBarFull + *s), (li / kRing) & 1u, abort_flag, p.err, lim))
+          return false;
+        tc_fence_after();
+        return true;
+      };
       auto pv = [&](int j) -> bool {  // O (+)= P(j) V(j)
         if (!mbar_wait_warp(bar(kBarP + (j & 1)), (uint32_t)(j >> 1) & 1u, abort_flag, p.err, lim))
           return false;
-        if (!mbar_wait_warp(bar(kBarVFull), (uint32_t)j & 1u, abort_flag, p.err, lim))
-          return false;
-        tc_fence_after();
         const uint32_t tP = tmem + kColS + (uint32_t)((j & 1) * kBN);
-        // 64 keys = 4 steps of 16 (2048 B apart); N = 256 spans the 4 chunks of
-        // this CTA's V half (LBO = one chunk).
-        mma4_ts<2048 / 16>(tO, tP, sdesc_sw128(sbase + kSmemV, kKChunk, 1024), kIdescPV,
-                           j > 0 ? 1u : 0u);
-        tc_commit_elect(bar(kBarVEmpty));
+        for (int h = 0; h < 2; ++h) {
+          uint32_t s0, s1;
+          if (!slot_ready(&s0)) return false;
+          ++li;
+          if (!slot_ready(&s1)) return false;
+          ++li;
+          // 64 keys = 4 steps of 16 (2048 B apart); N = 256 spans the 4
+          // 64-column chunks of this CTA's V half (LBO = one chunk, 8 KB)
+          mma4_ts<2048 / 16>(tO, tP + 32u * h, sdesc_sw128(sbase + kSmemRing + s0 * kSlot, kVSub, 1024),
+                             kIdescPV, (j > 0 || h > 0) ? 1u : 0u);
+          tc_commit_elect(bar(kBarEmpty + s0));
+          tc_commit_elect(bar(kBarEmpty + s1));
+        }
         tc_commit_elect(bar(kBarO));
         return true;
       };
@@ -231,14 +253,14 @@ bf16_d512_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
         const uint32_t tS = tmem + kColS + (uint32_t)((i & 1) * kBN);
 #pragma unroll 1
         for (int c = 0; c < 8 && ok; ++c) {
-          if (!(ok = mbar_wait_warp(bar(kBarKFull + c), (uint32_t)i & 1u, abort_flag, p.err, lim)))
-            break;
-          tc_fence_after();
+          uint32_t s;
+          if (!(ok = slot_ready(&s))) break;
           mma4_ss_kmajor(tS, sdesc_sw128(sbase + kSmemQ + c * kQChunk, 16, 1024),
-                         sdesc_sw128(sbase + kSmemK + c * kKChunk, 16, 1024), kIdescQK,
+                         sdesc_sw128(sbase + kSmemRing + s * kSlot, 16, 1024), kIdescQK,
                          c > 0 ? 1u : 0u);
           issued = true;
-          tc_commit_elect(bar(kBarKEmpty + c));
+          tc_commit_elect(bar(kBarEmpty + s));
+          ++li;
         }
         if (!ok) break;
         tc_commit_elect(bar(kBarS + (i & 1)));
@@ -274,20 +296,26 @@ bf16_d512_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
       if (!(ok = __all_sync(0xffffffffu, ok))) break;
       tc_fence_after();
       const uint32_t tS = tmem + lane_off + kColS + (uint32_t)((i & 1) * kBN);
-      uint32_t r0[32], r1[32];
+      uint32_t r0[32], r1[32], r2[32], r3[32];  // four loads in flight
       tmem_ld32(tS, r0);
       tmem_ld32(tS + 32, r1);
+      tmem_ld32(tS + 64, r2);
+      tmem_ld32(tS + 96, r3);
       tmem_wait_ld(r0);
       tmem_wait_ld(r1);
-      float x[64];
+      tmem_wait_ld(r2);
+      tmem_wait_ld(r3);
+      float x[128];
 #pragma unroll
       for (int j = 0; j < 32; ++j) {
         x[j] = __uint_as_float(r0[j]);
         x[32 + j] = __uint_as_float(r1[j]);
+        x[64 + j] = __uint_as_float(r2[j]);
+        x[96 + j] = __uint_as_float(r3[j]);
       }
       if (!kFoldScale) {
 #pragma unroll
-        for (int j = 0; j < 64; ++j) x[j] *= c;
+        for (int j = 0; j < 128; ++j) x[j] *= c;
       }
       const int64_t key0 = (kt_first + i) * kBN;
       const bool all_visible = (key0 + kBN - 1 <= pos_first) &&
@@ -296,16 +324,24 @@ bf16_d512_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
         const int64_t hi = pos - key0;
         const int64_t lo = p.window > 0 ? pos - p.window - key0 : -1;
 #pragma unroll
-        for (int j = 0; j < 64; ++j)
+        for (int j = 0; j < 128; ++j)
           if (j > hi || j <= lo) x[j] = -INFINITY;
       }
-      float pm[8];  // 8 independent partial max chains
+      // row max with three-input max instructions in 8 independent chains
+      float mx;
+      {
+        float m[8];
 #pragma unroll
-      for (int a = 0; a < 8; ++a) pm[a] = x[a];
+        for (int q = 0; q < 8; ++q) m[q] = max3f(x[q], x[8 + q], x[16 + q]);
 #pragma unroll
-      for (int j = 8; j < 64; ++j) pm[j & 7] = fmaxf(pm[j & 7], x[j]);
-      float mx = fmaxf(fmaxf(fmaxf(pm[0], pm[1]), fmaxf(pm[2], pm[3])),
-                       fmaxf(fmaxf(pm[4], pm[5]), fmaxf(pm[6], pm[7])));
+        for (int j = 24; j < 120; j += 16) {
+#pragma unroll
+          for (int q = 0; q < 8; ++q) m[q] = max3f(m[q], x[j + q], x[j + 8 + q]);
+        }
+#pragma unroll
+        for (int q = 0; q < 8; ++q) m[q] = fmaxf(m[q], x[120 + q]);
+        mx = max3f(max3f(m[0], m[1], m[2]), max3f(m[3], m[4], m[5]), fmaxf(m[6], m[7]));
+      }
       if (kFoldScale) mx *= c;
       float alpha = 1.f;
       bool rescale = false;
@@ -315,24 +351,23 @@ bf16_d512_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
         m_run = mx;
       }
       const float base = (m_run == -INFINITY) ? 0.f : m_run;
-      uint32_t pk[32];
-      float ps[8];  // 8 independent partial row sums (of the bf16-rounded P)
+      // P = 2^(s - base) as packed bf16 pairs; l gains the row sum of the
+      // unrounded values (8 independent partial sums)
+      uint32_t pk0[32], pk1[32];
+      float ls[8];
 #pragma unroll
-      for (int a = 0; a < 8; ++a) ps[a] = 0.f;
+      for (int q = 0; q < 8; ++q) ls[q] = 0.f;
 #pragma unroll
-      for (int j = 0; j < 32; ++j) {
-        float a, b;
-        if (kFoldScale) {
-          a = ex2(fmaf(x[2 * j], c, -base));
-          b = ex2(fmaf(x[2 * j + 1], c, -base));
-        } else {
-          a = ex2(x[2 * j] - base);
-          b = ex2(x[2 * j + 1] - base);
-        }
-        pk[j] = pack_bf16x2(a, b);
-        ps[j & 7] += bf16_lo(pk[j]) + bf16_hi(pk[j]);
+      for (int j = 0; j < 64; ++j) {
+        const float xa = x[2 * j], xb = x[2 * j + 1];
+        const float pa = kFoldScale ? ex2(fmaf(xa, c, -base)) : ex2(xa - base);
+        const float pb = kFoldScale ? ex2(fmaf(xb, c, -base)) : ex2(xb - base);
+        const uint32_t w = pack_bf16x2(pa, pb);
+        if (j < 32) pk0[j] = w; else pk1[j - 32] = w;
+        ls[(2 * j) & 7] += pa;
+        ls[(2 * j + 1) & 7] += pb;
       }
-      const float lsum = ((ps[0] + ps[1]) + (ps[2] + ps[3])) + ((ps[4] + ps[5]) + (ps[6] + ps[7]));
+      const float lsum = ((ls[0] + ls[1]) + (ls[2] + ls[3])) + ((ls[4] + ls[5]) + (ls[6] + ls[7]));
       l = l * alpha + lsum;
       if (i > 0) {
         // O (and the P buffer this tile reuses) are free once P(i-1) V is done.
@@ -352,7 +387,8 @@ bf16_d512_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
           tmem_st32(tO + c0, o);
         }
       }
-      tmem_st32(tS, pk);
+      tmem_st32(tS, pk0);
+      tmem_st32(tS + 32, pk1);
       tmem_wait_st();
       tc_fence_before();
       __syncwarp();
@@ -428,9 +464,10 @@ int launch_bf16_d512(const Call& c) {
     // Rows past the written part of the cache read as zeros.
     const uint64_t dims[3] = {512, (uint64_t)cache_rows_written(c), (uint64_t)c.Hkv};
     const uint64_t strides[2] = {512 * 2, (uint64_t)c.max_seq_len * 512 * 2};
-    const uint32_t box[3] = {64, (uint32_t)kBN, 1};
-    if (encode_tmap_bf16_3d(&tk, c.k, dims, strides, box)) return kErrLaunch;
-    if (encode_tmap_bf16_3d(&tv, c.v, dims, strides, box)) return kErrLaunch;
+    const uint32_t kbox[3] = {64, (uint32_t)kBN, 1};     // a K chunk: 128 keys x 64 columns
+    const uint32_t vbox[3] = {64, (uint32_t)kVKeys, 1};  // a V box: 64 keys x 64 columns
+    if (encode_tmap_bf16_3d(&tk, c.k, dims, strides, kbox)) return kErrLaunch;
+    if (encode_tmap_bf16_3d(&tv, c.v, dims, strides, vbox)) return kErrLaunch;
   }
   Params p;
   p.out = static_cast<__nv_bfloat16*>(c.out);
