@@ -158,6 +158,20 @@ class ClockSampler:
                 "reasons": sorted(reasons), "samples": len(sm)}
 
 
+def oracle_rate_1thread(wl, max_rows: int = 2048):
+    """fp64 oracle rate on one host thread over evenly spaced (token, head) rows."""
+    import oracle
+    from chunked_causal_gqa_gb300 import workloads as W
+
+    q, k, v = W.make_inputs(wl)
+    rows_all = [(t, h) for t in range(wl.T) for h in range(wl.num_heads)]
+    rows = rows_all[::max(1, len(rows_all) // max_rows)]
+    flops = sum(4.0 * wl.head_dim * _visible(wl, t) for t, _ in rows)
+    t0 = time.perf_counter()
+    oracle.prefill_attention_rows(q, k, v, rows, window=wl.window, scale=wl.scale, threads=1)
+    return flops / (time.perf_counter() - t0), len(rows)
+
+
 def oracle_sample(wl, budget_s: float):
     """Time the fp64 oracle on the host cores over a bounded sample of the
     workload's (token, head) rows.  Returns (flops/s, description, cores)."""
@@ -360,11 +374,23 @@ def run_ours(args, wl):
                                else "one step: one kernel launch"),
                 "algorithmic_bytes": wl.algorithmic_bytes(), **extra}
 
+    # bit-identical output across repeated runs (the determinism target)
+    digests = set()
+    for _ in range(5):
+        step()
+        torch.cuda.synchronize(dev)
+        digests.add(hashlib.sha256(out.contiguous().view(torch.uint8).cpu().numpy()
+                                   .tobytes()).hexdigest())
+
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         rate, descr, cores, _ = oracle_sample(wl, args.cpu_seconds)
         cpu = {"value": rate / 1e12, "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
                "sample": descr}
+        if wl.T * wl.num_heads <= 50000:   # the small configurations: also one thread
+            r1, n1 = oracle_rate_1thread(wl)
+            cpu["value_1thread"] = r1 / 1e12
+            cpu["sample_1thread"] = f"{n1} evenly spaced (token, head) rows, 1 thread"
 
     if rank == 0:
         line = {
@@ -383,6 +409,7 @@ def run_ours(args, wl):
             "ms_min": min(per), "ms_median": statistics.median(per),
             "wall_s_timed": wall,
             "gpu_launches": args.steps * (2 if ws_bytes > 0 else 1),
+            "output_sha256": sorted(digests)[0], "bit_identical_runs": 5 if len(digests) == 1 else 0,
             "schedule": sched_name,
             "workspace_bytes": ws_bytes,
             "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e, "clocks": clocks,

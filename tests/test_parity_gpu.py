@@ -326,3 +326,18 @@ def test_softmax_dynamic_range(profile, D):
     got = G.to_np(G.run(q, k, v))
     want = oracle.prefill_attention(q, k, v)
     G.check(got, want, "bf16", f"{profile} D{D}")
+
+
+def test_schedule_query_names_the_schedule_each_workload_gets():
+    import chunked_causal_gqa_gb300 as pkg
+    expect = {"mistral_1358": "plain", "chunk_64k": "tail", "chunk_128k": "tail",
+              "chunk_64k_t128": "balanced", "gemma_d512_global": "plain", "tiny_f32": "plain"}
+    for name, kind in expect.items():
+        wl = W.WORKLOADS[name]
+        got, nbytes = pkg.schedule(wl.T, wl.start_pos, wl.num_heads, wl.num_kv_heads,
+                                   wl.head_dim, wl.window, W.torch_dtype(wl.dtype))
+        assert got == kind, (name, got)
+        assert (nbytes > 0) == (kind != "plain")
+        assert nbytes == pkg.workspace_bytes(wl.T, wl.start_pos, wl.num_heads,
+                                             wl.num_kv_heads, wl.head_dim, wl.window,
+                                             W.torch_dtype(wl.dtype))
