@@ -174,7 +174,9 @@ def oracle_rate_1thread(wl, max_rows: int = 2048):
 
 def oracle_sample(wl, budget_s: float):
     """Time the fp64 oracle on the host cores over a bounded sample of the
-    workload's (token, head) rows.  Returns (flops/s, description, cores)."""
+    workload's (token, head) rows.  Returns (flops/s, description, cores,
+    seconds, rows, values): the rows timed and the oracle's outputs for them
+    (all rows in [T][H] order when the whole workload fits the budget)."""
     import numpy as np
 
     import oracle
@@ -200,17 +202,19 @@ def oracle_sample(wl, budget_s: float):
                                      max(flops_total / total_rows, 1.0))))
     if n_rows >= total_rows:
         t0 = time.perf_counter()
-        oracle.prefill_attention(q, k, v, window=wl.window, scale=wl.scale, threads=cores)
+        full = oracle.prefill_attention(q, k, v, window=wl.window, scale=wl.scale, threads=cores)
         dt = time.perf_counter() - t0
-        return flops_total / dt, f"full workload ({total_rows} rows)", cores, dt
+        return (flops_total / dt, f"full workload ({total_rows} rows)", cores, dt, rows_all,
+                full.reshape(total_rows, wl.head_dim))
     step = max(1, total_rows // n_rows)
     rows = rows_all[::step]
     sample_flops = sum(4.0 * wl.head_dim * _visible(wl, t) for t, _ in rows)
     t0 = time.perf_counter()
-    oracle.prefill_attention_rows(q, k, v, rows, window=wl.window, scale=wl.scale, threads=cores)
+    vals = oracle.prefill_attention_rows(q, k, v, rows, window=wl.window, scale=wl.scale,
+                                         threads=cores)
     dt = time.perf_counter() - t0
-    return sample_flops / dt, f"{len(rows)} of {total_rows} (token, head) rows, every {step}th", \
-        cores, dt
+    return (sample_flops / dt, f"{len(rows)} of {total_rows} (token, head) rows, every {step}th",
+            cores, dt, rows, vals)
 
 
 def _visible(wl, t):
@@ -226,7 +230,7 @@ def run_reference(args, wl):
     budget = max(1.0, args.ref_seconds / max(1, args.steps + args.warmup))
     flops_s = []
     for i in range(args.warmup + args.steps):
-        rate, descr, cores, dt = oracle_sample(wl, budget)
+        rate, descr, cores, dt, _, _ = oracle_sample(wl, budget)
         if i >= args.warmup:
             flops_s.append(rate)
             times.append(dt)
@@ -384,9 +388,14 @@ def run_ours(args, wl):
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        rate, descr, cores, _ = oracle_sample(wl, args.cpu_seconds)
+        rate, descr, cores, _, rows, vals = oracle_sample(wl, args.cpu_seconds)
         cpu = {"value": rate / 1e12, "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
                "sample": descr}
+        # the GPU output on the same rows against the oracle's values
+        import numpy as np
+        o = out.float().cpu().numpy().astype(np.float64)
+        got = o[[t for t, _ in rows], [h for _, h in rows]]
+        cpu["max_abs_err_vs_gpu"] = float(np.abs(got - vals).max())
         if wl.T * wl.num_heads <= 50000:   # the small configurations: also one thread
             r1, n1 = oracle_rate_1thread(wl)
             cpu["value_1thread"] = r1 / 1e12

@@ -26,7 +26,8 @@ EXPORTS = ("pfa_prefill_attention", "pfa_prefill_attention_ws", "pfa_workspace_b
            "pfa_prefill_attention_noalloc", "pfa_prefill_attention_cache",
            "pfa_prefill_attention_graph", "pfa_schedule",
            "pfa_status_string",
-           "pfa_last_device_error", "pfa_version", "pfa_debug_configure")
+           "pfa_last_device_error", "pfa_version", "pfa_debug_configure",
+           "pfa_debug_check_schedule")
 
 _lock = threading.Lock()
 _lib = None
@@ -83,6 +84,9 @@ def load(path: str | None = None) -> ctypes.CDLL:
         lib.pfa_version.restype = i32
         lib.pfa_debug_configure.argtypes = [ctypes.c_double, i32]
         lib.pfa_debug_configure.restype = i32
+        ip = ctypes.POINTER(i32)
+        lib.pfa_debug_check_schedule.argtypes = [i64, i64, i32, i32, i32, i32, ip, ip, ip]
+        lib.pfa_debug_check_schedule.restype = i32
         if path is None:
             _lib = lib
         return lib

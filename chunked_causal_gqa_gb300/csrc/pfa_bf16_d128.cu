@@ -926,6 +926,112 @@ bool choose_schedule(const Shape& s, int sms, Plan* plan) {
 
 }  // namespace
 
+// Host replay of the kernel's work assignment for one shape and SM count,
+// with the invariants every schedule must keep (see pfa_debug_check_schedule
+// in include/pfa.h).  Returns 0, or the number of the first failed check.
+int check_schedule_bf16_d128(const Call& c, int sms, int* schedule, int* ctas) {
+  Shape s;
+  if (!make_shape(c, &s)) return 1;
+  std::unique_ptr<Plan> plan(new Plan());
+  if (!choose_schedule(s, sms, plan.get())) {
+    plan->balanced = false;
+    plan->sched.mode = kPlain;
+    plan->grid = s.pairs;
+    plan->ws_bytes = 0;
+  }
+  const Sched& sc = plan->sched;
+  *schedule = sc.mode == kTail ? 2 : (sc.mode == kTable ? 1 : 0);
+  *ctas = plan->grid;
+  const std::vector<int> n = pair_tiles(s);
+  const int64_t L = s.start_pos + s.T;
+  // items of every CTA, as the kernel derives them
+  struct Got { int pair, kb, ke, slot; };
+  std::vector<Got> all;
+  for (int cta = 0; cta < plan->grid; ++cta) {
+    if (sc.mode == kTable) {
+      if (cta >= kMaxCtas || sc.cta_first[cta] > sc.cta_first[cta + 1] ||
+          sc.cta_first[cta + 1] > kMaxItems)
+        return 2;
+      for (int k = sc.cta_first[cta]; k < sc.cta_first[cta + 1]; ++k)
+        all.push_back({sc.items[k].pair, sc.items[k].kb, sc.items[k].ke, sc.items[k].slot});
+    } else if (sc.mode == kTail && cta >= sc.p1) {
+      const int j = cta - sc.p1, r = j / sc.p2, pair = sc.p1 + j % sc.p2;
+      if (pair >= s.pairs) return 3;
+      all.push_back({pair, (int)((int64_t)n[pair] * r / sc.parts),
+                     (int)((int64_t)n[pair] * (r + 1) / sc.parts), j});
+    } else {
+      if (cta >= s.pairs) return 3;
+      all.push_back({cta, 0, n[cta], -1});
+    }
+  }
+  // every key tile of every pair exactly once; whole-pair items direct,
+  // partial items in distinct slots that fit the workspace
+  std::vector<std::vector<std::pair<int, int>>> ranges(s.pairs);
+  std::vector<int> slot_used(kMaxPieces * 16, 0);
+  const size_t nslots = plan->ws_bytes / kSlotBytes;
+  for (const Got& g : all) {
+    if (g.pair < 0 || g.pair >= s.pairs || g.kb < 0 || g.ke > n[g.pair] || g.kb >= g.ke) return 4;
+    const bool whole = g.kb == 0 && g.ke == n[g.pair];
+    if (g.slot < 0 && !whole) return 5;
+    if (g.slot >= 0) {
+      if ((size_t)g.slot >= nslots || (size_t)g.slot >= slot_used.size() || slot_used[g.slot]++)
+        return 6;
+    }
+    ranges[g.pair].emplace_back(g.kb, g.ke);
+  }
+  for (int q = 0; q < s.pairs; ++q) {
+    std::sort(ranges[q].begin(), ranges[q].end());
+    int at = 0;
+    for (const auto& r : ranges[q]) {
+      if (r.first != at) return 7;
+      at = r.second;
+    }
+    if (at != n[q]) return 7;
+    // key coordinates of the pair's tiles stay inside the cache, and each
+    // tile holds a key some row of the pair sees
+    const Unit u = unit_of(s.T, s.start_pos, s.Hkv, s.tok_per_tile, s.window, s.units_per_head, q);
+    if (u.t0A < 0 || u.t0A >= s.T) return 8;
+    const int64_t pos_lo = s.start_pos + u.t0A;
+    const int64_t kmin = s.window > 0 ? std::max<int64_t>(0, pos_lo - s.window + 1) : 0;
+    for (int i = 0; i < n[q]; ++i) {
+      const int64_t key0 = (u.kt_first + i) * kBN;
+      if (key0 < 0 || key0 >= L || key0 + kBN - 1 < kmin) return 9;
+    }
+  }
+  // the merge kernel sees every split pair once, with its pieces in key order
+  if (plan->balanced) {
+    const MergeSched& ms = plan->merge;
+    std::vector<int> merged(s.pairs, 0);
+    for (int e = 0; e < ms.num; ++e) {
+      int pair, count;
+      std::vector<int> slots;
+      if (ms.tail) {
+        pair = ms.p1 + e;
+        count = ms.parts;
+        for (int r = 0; r < count; ++r) slots.push_back(r * ms.p2 + e);
+      } else {
+        pair = ms.e[e].pair;
+        count = ms.e[e].count;
+        for (int r = 0; r < count; ++r) slots.push_back(ms.slots[ms.e[e].first + r]);
+      }
+      if (pair < 0 || pair >= s.pairs || merged[pair]++) return 10;
+      std::vector<std::pair<int, int>> pieces;  // (kb, slot) of the pair's partial items
+      for (const Got& g : all)
+        if (g.pair == pair && g.slot >= 0) pieces.emplace_back(g.kb, g.slot);
+      std::sort(pieces.begin(), pieces.end());
+      if ((int)pieces.size() != count) return 11;
+      for (int r = 0; r < count; ++r)
+        if (pieces[r].second != slots[r]) return 11;
+    }
+    for (int q = 0; q < s.pairs; ++q)
+      if ((ranges[q].size() > 1) != (merged[q] > 0)) return 12;
+  } else {
+    for (const Got& g : all)
+      if (g.slot >= 0) return 12;
+  }
+  return 0;
+}
+
 size_t workspace_bytes_bf16_d128(const Call& c, int* schedule) {
   if (schedule) *schedule = 0;
   Shape s;

@@ -81,5 +81,8 @@ int launch_bf16_d128(const Call& c);
 // schedule); *schedule (if not null) gets 0 plain, 1 balanced, 2 tail split.
 size_t workspace_bytes_bf16_d128(const Call& c, int* schedule = nullptr);
 int launch_bf16_d512(const Call& c);
+// Host-only replay of the head_dim-128 work assignment with its invariants
+// (pfa_debug_check_schedule); 0 or the number of the failed check.
+int check_schedule_bf16_d128(const Call& c, int sms, int* schedule, int* ctas);
 
 }  // namespace pfa

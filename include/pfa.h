@@ -316,6 +316,26 @@ PFA_API const char *pfa_status_string(int status);
  */
 PFA_API int pfa_last_device_error(void *stream);
 
+/*
+ * pfa_debug_check_schedule -- test hook, host only (no device is touched):
+ * replays, for the bf16 head_dim-128 path of this shape on a GPU with
+ * `num_sms` SMs, the work assignment the kernels would execute with a large
+ * enough workspace -- every CTA's (query-tile pair, key-tile range, partial
+ * slot) items and the merge entries -- and checks its invariants: each key
+ * tile of each pair is computed exactly once, key tiles lie inside the cache
+ * and hold a visible key, whole-pair items write the output and partial items
+ * own distinct workspace slots that fit the workspace, and the merge combines
+ * exactly the split pairs' pieces in key order.
+ *   schedule      out: PFA_SCHEDULE_* of the shape
+ *   ctas          out: CTAs of the main kernel
+ *   failed_check  out: 0 when every invariant holds, else the number of the
+ *                 first failed check
+ * Returns PFA_OK (with the outputs set), PFA_ERR_NULL or PFA_ERR_SHAPE.
+ */
+PFA_API int pfa_debug_check_schedule(int64_t T, int64_t start_pos, int num_heads,
+                                     int num_kv_heads, int window, int num_sms, int *schedule,
+                                     int *ctas, int *failed_check);
+
 /* Library ABI version: (major << 16) | minor. */
 PFA_API int pfa_version(void);
 
