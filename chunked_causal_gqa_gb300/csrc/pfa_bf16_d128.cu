@@ -926,6 +926,41 @@ bool choose_schedule(const Shape& s, int sms, Plan* plan) {
 
 }  // namespace
 
+// Workspace schedules, cached per shape: planning simulates the SMs (tens of
+// microseconds for long chunks), and callers repeat shapes layer after layer.
+// A null entry means the plain schedule.  Most recently used first.
+struct PlanKey {
+  int64_t T, start_pos;
+  int H, Hkv, window, sms;
+  bool operator==(const PlanKey& o) const {
+    return T == o.T && start_pos == o.start_pos && H == o.H && Hkv == o.Hkv &&
+           window == o.window && sms == o.sms;
+  }
+};
+constexpr size_t kPlanCacheEntries = 32;
+std::mutex g_plan_mutex;
+std::vector<std::pair<PlanKey, std::shared_ptr<const Plan>>> g_plans;
+
+std::shared_ptr<const Plan> workspace_plan(const Shape& s, int sms) {
+  const PlanKey key{s.T, s.start_pos, s.H, s.Hkv, s.window, sms};
+  {
+    std::lock_guard<std::mutex> lk(g_plan_mutex);
+    for (size_t i = 0; i < g_plans.size(); ++i)
+      if (g_plans[i].first == key) {
+        std::shared_ptr<const Plan> hit = g_plans[i].second;
+        std::rotate(g_plans.begin(), g_plans.begin() + i, g_plans.begin() + i + 1);
+        return hit;
+      }
+  }
+  std::shared_ptr<Plan> plan = std::make_shared<Plan>();
+  std::shared_ptr<const Plan> made;
+  if (choose_schedule(s, sms, plan.get())) made = plan;
+  std::lock_guard<std::mutex> lk(g_plan_mutex);
+  g_plans.insert(g_plans.begin(), {key, made});
+  if (g_plans.size() > kPlanCacheEntries) g_plans.pop_back();
+  return made;
+}
+
 // Host replay of the kernel's work assignment for one shape and SM count,
 // with the invariants every schedule must keep (see pfa_debug_check_schedule
 // in include/pfa.h).  Returns 0, or the number of the first failed check.
@@ -1036,8 +1071,8 @@ size_t workspace_bytes_bf16_d128(const Call& c, int* schedule) {
   if (schedule) *schedule = 0;
   Shape s;
   if (!make_shape(c, &s)) return 0;
-  std::unique_ptr<Plan> plan(new Plan());
-  if (!choose_schedule(s, c.num_sms, plan.get())) return 0;
+  const std::shared_ptr<const Plan> plan = workspace_plan(s, c.num_sms);
+  if (!plan) return 0;
   if (schedule) *schedule = plan->sched.mode == kTail ? 2 : 1;
   return plan->ws_bytes;
 }
@@ -1067,14 +1102,20 @@ int launch_bf16_d128(const Call& c) {
   Shape s;
   if (!make_shape(c, &s)) return kErrShape;
 
-  // The schedule tables are ~20 KB: built per call on the heap.
-  std::unique_ptr<Plan> plan(new Plan());
-  if (!(c.ws != nullptr && c.lens == nullptr && choose_schedule(s, c.num_sms, plan.get()) &&
-        plan->ws_bytes <= c.ws_bytes)) {
-    plan->balanced = false;
-    plan->sched.mode = kPlain;
-    plan->grid = s.pairs;
+  // A workspace schedule when the caller gave a large enough workspace, else
+  // the plain one (its tables are unused: a shared, zeroed copy).
+  std::shared_ptr<const Plan> wplan;
+  if (c.ws != nullptr && c.lens == nullptr) {
+    wplan = workspace_plan(s, c.num_sms);
+    if (wplan && wplan->ws_bytes > c.ws_bytes) wplan.reset();
   }
+  static const Plan* const plain_plan = [] {
+    Plan* pl = new Plan();  // kept for the process: its Sched is only a parameter block
+    pl->sched.mode = kPlain;
+    return pl;
+  }();
+  const Plan& plan = wplan ? *wplan : *plain_plan;
+  const int grid_ctas = wplan ? wplan->grid : s.pairs;
 
   CUtensorMap tq, tk, tv;
   {
@@ -1110,27 +1151,27 @@ int launch_bf16_d128(const Call& c) {
   p.err = c.err;
   p.wait_limit_ns = c.wait_limit_ns;
   p.flags = c.flags;
-  const dim3 grid((unsigned)plan->grid);
+  const dim3 grid((unsigned)grid_ctas);
   const bool fold = p.scale_log2 > 0.f;
   if (c.lens) {
     if (fold)
       bf16_d128_kernel<true, true><<<grid, kThreads, kSmemAlloc, c.stream>>>(tq, tk, tv, p,
-                                                                           plan->sched);
+                                                                           plan.sched);
     else
       bf16_d128_kernel<false, true><<<grid, kThreads, kSmemAlloc, c.stream>>>(tq, tk, tv, p,
-                                                                            plan->sched);
+                                                                            plan.sched);
   } else if (fold) {
     bf16_d128_kernel<true, false><<<grid, kThreads, kSmemAlloc, c.stream>>>(tq, tk, tv, p,
-                                                                          plan->sched);
+                                                                          plan.sched);
   } else {
     bf16_d128_kernel<false, false><<<grid, kThreads, kSmemAlloc, c.stream>>>(tq, tk, tv, p,
-                                                                           plan->sched);
+                                                                           plan.sched);
   }
   if (cudaGetLastError() != cudaSuccess) return kErrLaunch;
-  if (plan->balanced && plan->merge.num > 0) {
-    merge_kernel<<<dim3((unsigned)plan->merge.num, 128 / kMergeCols), kPairRows, 0,
+  if (wplan && wplan->balanced && wplan->merge.num > 0) {
+    merge_kernel<<<dim3((unsigned)wplan->merge.num, 128 / kMergeCols), kPairRows, 0,
                    c.stream>>>(
-        p, plan->merge);
+        p, wplan->merge);
     if (cudaGetLastError() != cudaSuccess) return kErrLaunch;
   }
   return kOk;
