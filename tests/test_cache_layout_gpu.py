@@ -152,3 +152,10 @@ def test_cache_layout_errors():
     assert e.value.name == "PFA_ERR_ALIGNMENT"
     torch.cuda.synchronize()
     assert pkg.last_device_error() == 0
+
+
+def test_ring_cache_with_the_tail_split():
+    """The tail-split schedule reading a wrapped circular cache."""
+    T, sp, H, Hkv, D, window, cap = 1280, 60000, 32, 8, 128, 1024, 2304
+    assert pkg.schedule(T, sp, H, Hkv, D, window)[0] == "tail"
+    _run_case(T, sp, H, Hkv, D, window, "bf16", 0, cap, True, workspace="auto", seed=1234)

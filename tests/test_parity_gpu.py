@@ -341,3 +341,18 @@ def test_schedule_query_names_the_schedule_each_workload_gets():
         assert nbytes == pkg.workspace_bytes(wl.T, wl.start_pos, wl.num_heads,
                                              wl.num_kv_heads, wl.head_dim, wl.window,
                                              W.torch_dtype(wl.dtype))
+
+
+def test_tail_split_on_a_windowed_layer():
+    """A long windowed chunk deep in a cache larger than L2 takes the tail split."""
+    import chunked_causal_gqa_gb300 as pkg
+    H, Hkv, D, T, sp, w = 32, 8, 128, 1280, 60000, 1024
+    assert pkg.schedule(T, sp, H, Hkv, D, w)[0] == "tail"
+    q, k, v = W.make_random(T, sp, H, Hkv, D, "bf16", seed=77, q_std=1.0, kv_std=0.5)
+    got = G.run(q, k, v, window=w)
+    rows = G.sample_rows(T, H, 48, seed=77)
+    want = oracle.prefill_attention_rows(q, k, v, rows, window=w)
+    G.check(G.to_np(got)[[t for t, _ in rows], [h for _, h in rows]], want, "bf16", "tail+window")
+    plain = G.run(q, k, v, window=w, workspace=None)
+    G.check(G.to_np(plain)[[t for t, _ in rows], [h for _, h in rows]], want, "bf16",
+            "plain+window")
