@@ -130,3 +130,19 @@ def test_graph_entry_validation_without_gpu(lib):
     assert g(max_T=600) == -2                              # max_T > max_seq_len
     assert g(ring=1, w=0) == -2
     assert g(max_T=0) == 0                                 # no-op
+
+
+def test_c_program_uses_the_abi_without_a_gpu(lib, tmp_path):
+    """include/pfa.h compiles as C and the library links into a plain C program."""
+    import shutil
+    import subprocess
+    if shutil.which("gcc") is None:
+        pytest.skip("gcc not available")
+    here = os.path.dirname(os.path.abspath(__file__))
+    libdir = os.path.dirname(_binding.LIB_PATH)
+    exe = tmp_path / "abi_check"
+    subprocess.run(["gcc", "-std=c99", "-Wall", "-Werror", "-I", os.path.join(here, "..", "include"),
+                    os.path.join(here, "c_abi", "abi_check.c"), "-L", libdir, "-lpfa",
+                    "-Wl,-rpath," + libdir, "-o", str(exe)], check=True)
+    r = subprocess.run([str(exe)], capture_output=True, text=True)
+    assert r.returncode == 0, r.stderr

@@ -37,7 +37,7 @@ def _draw_case(rng):
                 seed=int(rng.integers(0, 100000)))
 
 
-CASES = [_draw_case(np.random.default_rng(9000 + i)) for i in range(40)]
+CASES = [_draw_case(np.random.default_rng(9000 + i)) for i in range(100)]
 
 
 @pytest.mark.parametrize("case", CASES, ids=lambda c: "{entry}_{dtype}_D{D}_H{H}_Hkv{Hkv}_T{T}_sp{sp}_w{window}".format(**c))
