@@ -70,6 +70,7 @@ F32_CASES = [
     (8, 2, 128, 300, 500, 65),     # window band crossing key tiles
     (8, 2, 128, 64, 3000, 0),      # short chunk deep in the cache
     (32, 8, 128, 200, 1000, 0),    # Mistral-like heads
+    (256, 1, 128, 3, 5, 0),        # group 256: too large for a tile, the CUDA-core kernel
 ]
 
 
