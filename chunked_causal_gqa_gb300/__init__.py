@@ -14,6 +14,7 @@ to and from the device when it is handed CPU tensors.
 """
 from __future__ import annotations
 
+import functools
 import math
 
 import torch
@@ -27,6 +28,12 @@ __all__ = ["prefill_attention", "prefill_attention_cache", "prefill_attention_gr
            "PFA_F32", "PFA_BF16"]
 
 _DTYPES = {torch.float32: PFA_F32, torch.bfloat16: PFA_BF16}
+
+
+@functools.lru_cache(maxsize=None)
+def _default_scale(head_dim: int) -> float:
+    """1/sqrt(head_dim) rounded to float32 (the configurations' scale)."""
+    return float(torch.tensor(1.0 / math.sqrt(head_dim), dtype=torch.float32))
 
 
 def _stream_handle(device: torch.device, stream) -> int:
@@ -101,7 +108,7 @@ def prefill_attention(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Ten
     if start_pos < 0 or start_pos + T != L:
         raise ValueError(f"cache length {L} must equal start_pos + T = {start_pos + T}")
     if scale is None:
-        scale = float(torch.tensor(1.0 / math.sqrt(D), dtype=torch.float32))
+        scale = _default_scale(D)
 
     host = q.device.type == "cpu"
     if host:
@@ -195,7 +202,7 @@ def prefill_attention_cache(q: torch.Tensor, k_cache: torch.Tensor, v_cache: tor
             or (T > 1 and out.stride() != q.stride())):
         raise ValueError("out must match q in shape, strides, dtype and device")
     if scale is None:
-        scale = float(torch.tensor(1.0 / math.sqrt(D), dtype=torch.float32))
+        scale = _default_scale(D)
     dev = q.device
     lib = _binding.load()
     with torch.cuda.device(dev):
@@ -258,7 +265,7 @@ def prefill_attention_graph(q: torch.Tensor, k_cache: torch.Tensor, v_cache: tor
             or (max_T > 1 and out.stride() != q.stride())):
         raise ValueError("out must match q in shape, strides and dtype")
     if scale is None:
-        scale = float(torch.tensor(1.0 / math.sqrt(D), dtype=torch.float32))
+        scale = _default_scale(D)
     dev = q.device
     lib = _binding.load()
     with torch.cuda.device(dev):

@@ -43,6 +43,8 @@ class PfaError(RuntimeError):
 def load(path: str | None = None) -> ctypes.CDLL:
     """Load libpfa.so (raises if it is missing: build it with build.build())."""
     global _lib
+    if _lib is not None and path is None:      # loaded: no lock on the call path
+        return _lib
     with _lock:
         if _lib is not None and path is None:
             return _lib
