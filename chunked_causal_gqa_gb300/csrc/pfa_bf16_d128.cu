@@ -135,6 +135,18 @@ struct Sched {
   int cta_first[kMaxCtas + 1];
   Item items[kMaxItems];
 };
+// The plain and tail-split modes need only the head of the schedule.  Their
+// kernels take this 16-byte block instead of the ~9 KB table: the large
+// parameter block costs launch time, and the table code left the hot loop
+// short of registers (spills).
+struct SchedLite {
+  int mode;
+  int p1, p2, parts;
+};
+__device__ __forceinline__ int table_first(const Sched& s, int c) { return s.cta_first[c]; }
+__device__ __forceinline__ int table_first(const SchedLite&, int) { return 0; }
+__device__ __forceinline__ Item table_item(const Sched& s, int k) { return s.items[k]; }
+__device__ __forceinline__ Item table_item(const SchedLite&, int) { return Item{0, 0, 0, -1}; }
 struct MergeEntry {
   int pair, first, count, pad;  // pieces slots[first .. first+count), in key order
 };
@@ -145,6 +157,17 @@ struct MergeSched {
   MergeEntry e[kMaxMerge];
   int slots[kMaxPieces];
 };
+
+// The tail-split merge needs only the head.
+struct MergeLite {
+  int num, tail, p1, p2, parts;
+};
+__device__ __forceinline__ MergeEntry merge_entry(const MergeSched& ms, int b) { return ms.e[b]; }
+__device__ __forceinline__ MergeEntry merge_entry(const MergeLite&, int) {
+  return MergeEntry{0, 0, 0, 0};
+}
+__device__ __forceinline__ int merge_slot(const MergeSched& ms, int i) { return ms.slots[i]; }
+__device__ __forceinline__ int merge_slot(const MergeLite&, int) { return 0; }
 
 struct Params {
   __nv_bfloat16* out;
@@ -189,11 +212,11 @@ __device__ __forceinline__ Unit unit_of(const Params& p, int pidx) {
   return unit_of(p.T, p.start_pos, p.Hkv, p.tok_per_tile, p.window, p.units_per_head, pidx);
 }
 
-template <bool kFoldScale, bool kDyn>
+template <bool kFoldScale, bool kDyn, typename SchedT>
 __global__ void __launch_bounds__(kThreads, 1)
 bf16_d128_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                  const __grid_constant__ CUtensorMap tm_v, const Params p,
-                 const __grid_constant__ Sched sched) {
+                 const __grid_constant__ SchedT sched) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -223,11 +246,12 @@ bf16_d128_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
   auto unit = [&](int pidx) -> Unit {
     return unit_of(T, start_pos, p.Hkv, p.tok_per_tile, p.window, units_per_head, pidx);
   };
-  const bool table = (sched.mode == kTable);
-  const int item_begin = table ? sched.cta_first[cta] : 0;
-  const int item_end = table ? sched.cta_first[cta + 1] : 1;
+  constexpr bool kHasTable = sizeof(SchedT) > sizeof(SchedLite);
+  const bool table = kHasTable && (sched.mode == kTable);
+  const int item_begin = table ? table_first(sched, cta) : 0;
+  const int item_end = table ? table_first(sched, cta + 1) : 1;
   auto get_item = [&](int k) -> Item {
-    if (table) return sched.items[k];
+    if (table) return table_item(sched, k);
     Item it;
     if (sched.mode == kTail && cta >= sched.p1) {
       const int j = cta - sched.p1, r = j / sched.p2;
@@ -593,18 +617,19 @@ bf16_d128_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
 constexpr int kMergeCols = 16;
 constexpr int kMergeUnroll = 4;
 
+template <typename MS>
 __global__ void __launch_bounds__(kPairRows)
-merge_kernel(const Params p, const __grid_constant__ MergeSched ms) {
+merge_kernel(const Params p, const __grid_constant__ MS ms) {
   MergeEntry e;
   if (ms.tail) {
     e.pair = ms.p1 + (int)blockIdx.x;
     e.first = 0;
     e.count = ms.parts;
   } else {
-    e = ms.e[blockIdx.x];
+    e = merge_entry(ms, (int)blockIdx.x);
   }
   auto slot_of = [&](int i) -> int {
-    return ms.tail ? i * ms.p2 + (int)blockIdx.x : ms.slots[e.first + i];
+    return ms.tail ? i * ms.p2 + (int)blockIdx.x : merge_slot(ms, e.first + i);
   };
   const Unit u = unit_of(p, e.pair);
   const int R = threadIdx.x;
@@ -1089,10 +1114,12 @@ int launch_bf16_d128(const Call& c) {
   static int attr_state[64] = {0};  // 0: not checked, 1: ok, -1: unusable
   if (c.device < 0 || c.device >= 64) return kErrDevice;
   if (attr_state[c.device] == 0) {
-    const bool ok = setup_kernel((const void*)bf16_d128_kernel<true, false>) == kOk &&
-                    setup_kernel((const void*)bf16_d128_kernel<false, false>) == kOk &&
-                    setup_kernel((const void*)bf16_d128_kernel<true, true>) == kOk &&
-                    setup_kernel((const void*)bf16_d128_kernel<false, true>) == kOk;
+    const bool ok = setup_kernel((const void*)bf16_d128_kernel<true, false, SchedLite>) == kOk &&
+                    setup_kernel((const void*)bf16_d128_kernel<false, false, SchedLite>) == kOk &&
+                    setup_kernel((const void*)bf16_d128_kernel<true, false, Sched>) == kOk &&
+                    setup_kernel((const void*)bf16_d128_kernel<false, false, Sched>) == kOk &&
+                    setup_kernel((const void*)bf16_d128_kernel<true, true, SchedLite>) == kOk &&
+                    setup_kernel((const void*)bf16_d128_kernel<false, true, SchedLite>) == kOk;
     attr_state[c.device] = ok ? 1 : -1;
   }
   if (attr_state[c.device] != 1) {
@@ -1103,19 +1130,16 @@ int launch_bf16_d128(const Call& c) {
   if (!make_shape(c, &s)) return kErrShape;
 
   // A workspace schedule when the caller gave a large enough workspace, else
-  // the plain one (its tables are unused: a shared, zeroed copy).
+  // the plain one.
   std::shared_ptr<const Plan> wplan;
   if (c.ws != nullptr && c.lens == nullptr) {
     wplan = workspace_plan(s, c.num_sms);
     if (wplan && wplan->ws_bytes > c.ws_bytes) wplan.reset();
   }
-  static const Plan* const plain_plan = [] {
-    Plan* pl = new Plan();  // kept for the process: its Sched is only a parameter block
-    pl->sched.mode = kPlain;
-    return pl;
-  }();
-  const Plan& plan = wplan ? *wplan : *plain_plan;
   const int grid_ctas = wplan ? wplan->grid : s.pairs;
+  const bool table = wplan && wplan->sched.mode == kTable;
+  SchedLite lite{kPlain, 0, 0, 0};
+  if (wplan) lite = SchedLite{wplan->sched.mode, wplan->sched.p1, wplan->sched.p2, wplan->sched.parts};
 
   CUtensorMap tq, tk, tv;
   {
@@ -1155,23 +1179,34 @@ int launch_bf16_d128(const Call& c) {
   const bool fold = p.scale_log2 > 0.f;
   if (c.lens) {
     if (fold)
-      bf16_d128_kernel<true, true><<<grid, kThreads, kSmemAlloc, c.stream>>>(tq, tk, tv, p,
-                                                                           plan.sched);
+      bf16_d128_kernel<true, true, SchedLite>
+          <<<grid, kThreads, kSmemAlloc, c.stream>>>(tq, tk, tv, p, lite);
     else
-      bf16_d128_kernel<false, true><<<grid, kThreads, kSmemAlloc, c.stream>>>(tq, tk, tv, p,
-                                                                            plan.sched);
+      bf16_d128_kernel<false, true, SchedLite>
+          <<<grid, kThreads, kSmemAlloc, c.stream>>>(tq, tk, tv, p, lite);
+  } else if (table) {
+    if (fold)
+      bf16_d128_kernel<true, false, Sched>
+          <<<grid, kThreads, kSmemAlloc, c.stream>>>(tq, tk, tv, p, wplan->sched);
+    else
+      bf16_d128_kernel<false, false, Sched>
+          <<<grid, kThreads, kSmemAlloc, c.stream>>>(tq, tk, tv, p, wplan->sched);
   } else if (fold) {
-    bf16_d128_kernel<true, false><<<grid, kThreads, kSmemAlloc, c.stream>>>(tq, tk, tv, p,
-                                                                          plan.sched);
+    bf16_d128_kernel<true, false, SchedLite>
+        <<<grid, kThreads, kSmemAlloc, c.stream>>>(tq, tk, tv, p, lite);
   } else {
-    bf16_d128_kernel<false, false><<<grid, kThreads, kSmemAlloc, c.stream>>>(tq, tk, tv, p,
-                                                                           plan.sched);
+    bf16_d128_kernel<false, false, SchedLite>
+        <<<grid, kThreads, kSmemAlloc, c.stream>>>(tq, tk, tv, p, lite);
   }
   if (cudaGetLastError() != cudaSuccess) return kErrLaunch;
   if (wplan && wplan->balanced && wplan->merge.num > 0) {
-    merge_kernel<<<dim3((unsigned)wplan->merge.num, 128 / kMergeCols), kPairRows, 0,
-                   c.stream>>>(
-        p, wplan->merge);
+    const MergeSched& ms = wplan->merge;
+    const dim3 mgrid((unsigned)ms.num, 128 / kMergeCols);
+    if (ms.tail)
+      merge_kernel<MergeLite><<<mgrid, kPairRows, 0, c.stream>>>(
+          p, MergeLite{ms.num, ms.tail, ms.p1, ms.p2, ms.parts});
+    else
+      merge_kernel<MergeSched><<<mgrid, kPairRows, 0, c.stream>>>(p, ms);
     if (cudaGetLastError() != cudaSuccess) return kErrLaunch;
   }
   return kOk;
