@@ -102,7 +102,8 @@ constexpr int kBarP = kBarS + 2;             // 2
 constexpr int kBarO = kBarP + 2;             // 2: item's accumulators complete
 constexpr int kBarOFree = kBarO + 2;         // 2: item's epilogue has read O
 constexpr int kBarDrain = kBarOFree + 2;
-constexpr int kNumBars = kBarDrain + 1;
+constexpr int kBarQB = kBarDrain + 1;        // short launches: Q_B loaded (kBarQ then covers Q_A)
+constexpr int kNumBars = kBarQB + 1;
 constexpr int kOffTmemSlot = kNumBars * 8;
 constexpr int kOffAbort = kOffTmemSlot + 4;
 static_assert(kOffAbort + 4 <= 256, "barrier area");
@@ -129,6 +130,9 @@ struct Item {
 //            CTA p1 + r * p2 + e runs part r (of `parts` equal key ranges) of
 //            pair p1 + e into workspace slot r * p2 + e.
 constexpr int kPlain = 0, kTable = 1, kTail = 2;
+// Plain launches whose longest pair holds at most this many key tiles take
+// the short-launch kernel variant (kShort).
+constexpr int kShortTiles = 64;
 struct Sched {
   int mode;
   int p1, p2, parts;
@@ -212,7 +216,13 @@ __device__ __forceinline__ Unit unit_of(const Params& p, int pidx) {
   return unit_of(p.T, p.start_pos, p.Hkv, p.tok_per_tile, p.window, p.units_per_head, pidx);
 }
 
-template <bool kFoldScale, bool kDyn, typename SchedT>
+// kShort (launches whose pairs hold few key tiles, where the set-up and the
+// epilogue are a large part of each CTA): Q_B is loaded after the first K
+// tile, so the first product waits for half of the query rows only, and the
+// output is staged in the free Q buffer and written back in 512-byte runs.
+// The long launches keep the plain order and direct stores, which measured
+// ~1% faster there.
+template <bool kFoldScale, bool kDyn, typename SchedT, bool kShort>
 __global__ void __launch_bounds__(kThreads, 1)
 bf16_d128_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                  const __grid_constant__ CUtensorMap tm_v, const Params p,
@@ -297,19 +307,22 @@ bf16_d128_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
       // Each Q box is group x tok_per_tile rows of 128 bytes (zero-filled past T).
       const uint32_t q_bytes = 4u * 128u * (uint32_t)(p.group * p.tok_per_tile);
       uint32_t li = 0, nq = 0;
-      bool ok = true;
+      bool ok = true, qb_pending = false;
       for (int k = item_begin; k < item_end && ok; ++k) {
         const Item it = get_item(k);
         const Unit u = unit(it.pair);
         if (nq > 0 && !(ok = mbar_wait(bar(kBarQFree), (nq - 1) & 1u, abort_flag, p.err, lim)))
           break;
         const int hq = u.kh * p.group;
-        mbar_arrive_expect_tx(bar(kBarQ), q_bytes);
+        auto load_qb = [&](uint32_t b) {
+          tma_load_3d(sbase + kSmemQ + kTileBytes, &tm_q, b, 0, hq, (int)u.t0B);
+          tma_load_3d(sbase + kSmemQ + kTileBytes + kHalfBytes, &tm_q, b, 64, hq, (int)u.t0B);
+        };
+        mbar_arrive_expect_tx(bar(kBarQ), kShort ? q_bytes / 2 : q_bytes);
         tma_load_3d(sbase + kSmemQ, &tm_q, bar(kBarQ), 0, hq, (int)u.t0A);
         tma_load_3d(sbase + kSmemQ + kHalfBytes, &tm_q, bar(kBarQ), 64, hq, (int)u.t0A);
-        tma_load_3d(sbase + kSmemQ + kTileBytes, &tm_q, bar(kBarQ), 0, hq, (int)u.t0B);
-        tma_load_3d(sbase + kSmemQ + kTileBytes + kHalfBytes, &tm_q, bar(kBarQ), 64, hq,
-                    (int)u.t0B);
+        if (!kShort) load_qb(bar(kBarQ));
+        qb_pending = kShort;
         ++nq;
         for (int i = it.kb; i < it.ke && ok; ++i) {
           const int key0 = (int)((u.kt_first + i) * kBN);
@@ -324,12 +337,19 @@ bf16_d128_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
             tma_load_3d(dst, map, bar(kBarFull + s), 0, row0, u.kh);
             tma_load_3d(dst + kHalfBytes, map, bar(kBarFull + s), 64, row0, u.kh);
             ++li;
+            if (kShort && qb_pending) {  // Q_B right after the item's first K tile
+              qb_pending = false;
+              mbar_arrive_expect_tx(bar(kBarQB), q_bytes / 2);
+              load_qb(bar(kBarQB));
+            }
           }
         }
       }
       // No copy may be in flight when the CTA exits.  On the normal path the
       // MMA thread has already consumed every load, so these return at once.
       if (nq > 0) mbar_wait(bar(kBarQ), (nq - 1) & 1u, abort_flag, p.err, lim, true);
+      if (kShort && nq > 0 && !qb_pending)
+        mbar_wait(bar(kBarQB), (nq - 1) & 1u, abort_flag, p.err, lim, true);
       const uint32_t first = li > (uint32_t)kSlots ? li - kSlots : 0;
       for (uint32_t j = first; j < li; ++j)
         mbar_wait(bar(kBarFull + j % kSlots), (j / kSlots) & 1u, abort_flag, p.err, lim, true);
@@ -374,6 +394,10 @@ bf16_d128_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
             mma8_ts<2048 / 16>(tOB, tSB, sdesc_sw128(sbase + kSmemRing + vs * kTileBytes, kHalfBytes, 1024), kIdescPV,
                  (i - 1 > 0) ? 1u : 0u);
             tc_commit_elect(bar(kBarEmpty + vs));
+          }
+          if (kShort && i == 0) {
+            if (!(ok = mbar_wait_warp(bar(kBarQB), kk & 1u, abort_flag, p.err, lim))) break;
+            tc_fence_after();
           }
           mma8_ss_kmajor<kHalfBytes / 16>(tSB, qdB, sdesc_sw128(k_addr, 16, 1024), kIdescQK, 0);
           tc_commit_elect(bar(kBarS + 1));
@@ -555,7 +579,44 @@ bf16_d128_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
       const int64_t t = (int64_t)t0 + tok;
       const bool row_valid = row_exists && t < T;
       const int h = u.kh * p.group + hrow;
-      if (it.slot < 0) {
+      if (kShort && !kHasTable && it.slot < 0) {
+        // whole pair, the CTA's only item: this tile's Q buffer is free (every
+        // S_X product has completed), so each warp stages its 32 output rows
+        // there, 16-byte chunks rotated by row, and writes them back two rows
+        // (512 contiguous bytes) per store instead of 32 scattered 16-byte pieces.
+        const float inv = l > 0.f ? 1.f / l : 0.f;
+        uint8_t* wbuf = smem + kSmemQ + X * kTileBytes + wq * (32 * 256);
+#pragma unroll 1
+        for (int c0 = 0; c0 < 128; c0 += 32) {
+          uint32_t o[32];
+          tmem_ld32(tO + c0, o);
+          tmem_wait_ld(o);
+          uint32_t w[16];
+#pragma unroll
+          for (int j = 0; j < 16; ++j)
+            w[j] = pack_bf16x2(__uint_as_float(o[2 * j]) * inv, __uint_as_float(o[2 * j + 1]) * inv);
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            const int chunk = (c0 >> 3) + j;
+            *reinterpret_cast<uint4*>(wbuf + lane * 256 + ((chunk ^ (lane & 15)) << 4)) =
+                make_uint4(w[4 * j], w[4 * j + 1], w[4 * j + 2], w[4 * j + 3]);
+          }
+        }
+        __syncwarp();
+        const int ch = lane & 15;
+#pragma unroll 4
+        for (int i = 0; i < 16; ++i) {
+          const int rl = 2 * i + (lane >> 4);
+          const uint4 val =
+              *reinterpret_cast<const uint4*>(wbuf + rl * 256 + ((ch ^ (rl & 15)) << 4));
+          const int r = wq * 32 + rl;
+          const int tk = r / p.group;
+          const int64_t tt = (int64_t)t0 + tk;
+          if (tk < p.tok_per_tile && tt < T)
+            *reinterpret_cast<uint4*>(p.out + tt * p.o_stride +
+                                      (int64_t)(u.kh * p.group + r % p.group) * 128 + ch * 8) = val;
+        }
+      } else if (it.slot < 0) {
         // whole pair: normalise, round to bf16, store token-major
         const float inv = l > 0.f ? 1.f / l : 0.f;
         __nv_bfloat16* orow = p.out + (t * p.o_stride + h * (int64_t)128);
@@ -1114,12 +1175,17 @@ int launch_bf16_d128(const Call& c) {
   static int attr_state[64] = {0};  // 0: not checked, 1: ok, -1: unusable
   if (c.device < 0 || c.device >= 64) return kErrDevice;
   if (attr_state[c.device] == 0) {
-    const bool ok = setup_kernel((const void*)bf16_d128_kernel<true, false, SchedLite>) == kOk &&
-                    setup_kernel((const void*)bf16_d128_kernel<false, false, SchedLite>) == kOk &&
-                    setup_kernel((const void*)bf16_d128_kernel<true, false, Sched>) == kOk &&
-                    setup_kernel((const void*)bf16_d128_kernel<false, false, Sched>) == kOk &&
-                    setup_kernel((const void*)bf16_d128_kernel<true, true, SchedLite>) == kOk &&
-                    setup_kernel((const void*)bf16_d128_kernel<false, true, SchedLite>) == kOk;
+    const void* fns[] = {
+        (const void*)bf16_d128_kernel<true, false, SchedLite, false>,
+        (const void*)bf16_d128_kernel<false, false, SchedLite, false>,
+        (const void*)bf16_d128_kernel<true, false, SchedLite, true>,
+        (const void*)bf16_d128_kernel<false, false, SchedLite, true>,
+        (const void*)bf16_d128_kernel<true, false, Sched, false>,
+        (const void*)bf16_d128_kernel<false, false, Sched, false>,
+        (const void*)bf16_d128_kernel<true, true, SchedLite, false>,
+        (const void*)bf16_d128_kernel<false, true, SchedLite, false>};
+    bool ok = true;
+    for (const void* fn : fns) ok = ok && setup_kernel(fn) == kOk;
     attr_state[c.device] = ok ? 1 : -1;
   }
   if (attr_state[c.device] != 1) {
@@ -1177,25 +1243,35 @@ int launch_bf16_d128(const Call& c) {
   p.flags = c.flags;
   const dim3 grid((unsigned)grid_ctas);
   const bool fold = p.scale_log2 > 0.f;
+  // Short launches: plain schedule and at most kShortTiles key tiles per pair.
+  const bool short_launch = !wplan && unit_of(s.T, s.start_pos, s.Hkv, s.tok_per_tile, s.window,
+                                              s.units_per_head, 0).n <= kShortTiles;
   if (c.lens) {
     if (fold)
-      bf16_d128_kernel<true, true, SchedLite>
+      bf16_d128_kernel<true, true, SchedLite, false>
           <<<grid, kThreads, kSmemAlloc, c.stream>>>(tq, tk, tv, p, lite);
     else
-      bf16_d128_kernel<false, true, SchedLite>
+      bf16_d128_kernel<false, true, SchedLite, false>
           <<<grid, kThreads, kSmemAlloc, c.stream>>>(tq, tk, tv, p, lite);
   } else if (table) {
     if (fold)
-      bf16_d128_kernel<true, false, Sched>
+      bf16_d128_kernel<true, false, Sched, false>
           <<<grid, kThreads, kSmemAlloc, c.stream>>>(tq, tk, tv, p, wplan->sched);
     else
-      bf16_d128_kernel<false, false, Sched>
+      bf16_d128_kernel<false, false, Sched, false>
           <<<grid, kThreads, kSmemAlloc, c.stream>>>(tq, tk, tv, p, wplan->sched);
+  } else if (short_launch) {
+    if (fold)
+      bf16_d128_kernel<true, false, SchedLite, true>
+          <<<grid, kThreads, kSmemAlloc, c.stream>>>(tq, tk, tv, p, lite);
+    else
+      bf16_d128_kernel<false, false, SchedLite, true>
+          <<<grid, kThreads, kSmemAlloc, c.stream>>>(tq, tk, tv, p, lite);
   } else if (fold) {
-    bf16_d128_kernel<true, false, SchedLite>
+    bf16_d128_kernel<true, false, SchedLite, false>
         <<<grid, kThreads, kSmemAlloc, c.stream>>>(tq, tk, tv, p, lite);
   } else {
-    bf16_d128_kernel<false, false, SchedLite>
+    bf16_d128_kernel<false, false, SchedLite, false>
         <<<grid, kThreads, kSmemAlloc, c.stream>>>(tq, tk, tv, p, lite);
   }
   if (cudaGetLastError() != cudaSuccess) return kErrLaunch;
