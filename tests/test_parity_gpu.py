@@ -83,6 +83,33 @@ def test_f32_small_full_parity(case):
     G.check(got, want, "f32", str(case))
 
 
+# The head_dim-128 bf16 kernel has two instances: plain launches whose longest
+# query-tile pair holds at most 64 key tiles of 128 keys (all the shapes
+# above) take the short-launch one (Q_A loaded before Q_B, output staged in
+# shared memory); longer ones take the other.  These shapes keep the long
+# instance under the same ragged / odd-group / window cases, and pin the
+# switch at exactly 64 and 65 key tiles (L = 8192 and 8193).
+LONG_BF16_CASES = [
+    (8, 2, 128, 64, 8128, 0),      # L = 8192: 64 key tiles, the short instance's limit
+    (8, 2, 128, 64, 8129, 0),      # L = 8193: 65 key tiles, the long instance
+    (6, 2, 128, 150, 9000, 0),     # group 3, ragged T
+    (16, 2, 128, 100, 9000, 0),    # group 8
+    (128, 1, 128, 5, 9000, 0),     # group 128: 1 token per tile
+    (8, 2, 128, 257, 8500, 0),     # one token past a tile
+    (8, 2, 128, 200, 9000, 8300),  # window wider than 64 key tiles
+]
+
+
+@pytest.mark.parametrize("workspace", [None, "auto"])
+@pytest.mark.parametrize("case", LONG_BF16_CASES, ids=lambda c: "H%d_Hkv%d_D%d_T%d_sp%d_w%d" % c)
+def test_bf16_long_instance_full_parity(case, workspace):
+    H, Hkv, D, T, sp, w = case
+    q, k, v = W.make_random(T, sp, H, Hkv, D, "bf16", seed=sum(case), q_std=1.0, kv_std=0.5)
+    got = G.to_np(G.run(q, k, v, window=w, workspace=workspace))
+    want = oracle.prefill_attention(q, k, v, window=w)
+    G.check(got, want, "bf16", str(case))
+
+
 def test_tiny_f32_workload_full_parity():
     wl = W.WORKLOADS["tiny_f32"]
     q, k, v = W.make_inputs(wl)
