@@ -16,6 +16,7 @@ from __future__ import annotations
 
 import functools
 import math
+import threading
 
 import torch
 
@@ -23,7 +24,7 @@ from . import _binding
 from ._binding import PFA_BF16, PFA_F32, PfaError
 
 __all__ = ["prefill_attention", "prefill_attention_cache", "prefill_attention_graph",
-           "workspace_bytes", "schedule",
+           "workspace_bytes", "schedule", "release_host_buffers",
            "last_device_error", "status_string", "version", "debug_configure", "PfaError",
            "PFA_F32", "PFA_BF16"]
 
@@ -89,9 +90,13 @@ def prefill_attention(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Ten
     the plain schedule (pfa_prefill_attention, no workspace).
 
     CUDA tensors: the call is enqueued on `stream` (default: the current
-    stream) and returns without synchronising.  CPU tensors: they are copied to
-    the current CUDA device, the kernel runs, and the result is copied back
-    (the copy back synchronises).
+    stream) and returns without synchronising.  CPU tensors (pinned for full
+    copy speed): pfa_prefill_attention_host copies them to the current CUDA
+    device into a device buffer the binding keeps for later calls
+    (release_host_buffers() frees it), overlapping the copies with the
+    kernels by groups of kv heads, copies the result back into `out` (a new
+    CPU tensor, pinned if q is, when out is None) and synchronises `stream`
+    before returning; `workspace` is not used there.
     """
     if q.dim() != 3 or k_cache.dim() != 3 or v_cache.dim() != 3:
         raise ValueError("q must be [T, H, D]; k_cache and v_cache [Hkv, L, D]")
@@ -110,21 +115,16 @@ def prefill_attention(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Ten
     if scale is None:
         scale = _default_scale(D)
 
-    host = q.device.type == "cpu"
-    if host:
-        dev = torch.device("cuda", torch.cuda.current_device())
-        qd = q.to(dev, non_blocking=True)
-        kd = k_cache.to(dev, non_blocking=True)
-        vd = v_cache.to(dev, non_blocking=True)
-        od = torch.empty_like(qd)
-    else:
-        if k_cache.device != q.device or v_cache.device != q.device:
-            raise ValueError("q, k_cache and v_cache must be on one device")
-        dev = q.device
-        qd, kd, vd = q, k_cache, v_cache
-        od = out if out is not None else torch.empty_like(q)
-        if od.shape != q.shape or od.dtype != q.dtype or od.device != q.device:
-            raise ValueError("out must match q in shape, dtype and device")
+    if k_cache.device != q.device or v_cache.device != q.device:
+        raise ValueError("q, k_cache and v_cache must be on one device")
+    if q.device.type == "cpu":
+        return _prefill_host(q, k_cache, v_cache, out, T, start_pos, H, Hkv, D, window, scale,
+                             stream)
+    dev = q.device
+    qd, kd, vd = q, k_cache, v_cache
+    od = out if out is not None else torch.empty_like(q)
+    if od.shape != q.shape or od.dtype != q.dtype or od.device != q.device:
+        raise ValueError("out must match q in shape, dtype and device")
     for name, t in (("q", qd), ("k_cache", kd), ("v_cache", vd), ("out", od)):
         if not t.is_contiguous():
             raise ValueError(f"{name} must be contiguous")
@@ -155,12 +155,64 @@ def prefill_attention(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Ten
             workspace.record_stream(stream)
     if rc != 0:
         raise PfaError(rc, "pfa_prefill_attention")
-    if host:
-        if out is not None:
-            out.copy_(od)          # device -> host (synchronises)
-            return out
-        return od.to("cpu")
     return od
+
+
+# Device buffers of the host path, one per device, kept for reuse by later
+# calls (grown when a call needs more); the lock keeps two threads from using
+# one buffer at the same time.  release_host_buffers() returns them.
+_host_lock = threading.Lock()
+_host_bufs: dict = {}
+
+
+def release_host_buffers() -> None:
+    """Free the device buffers kept by prefill_attention on CPU tensors."""
+    with _host_lock:
+        _host_bufs.clear()
+
+
+def _prefill_host(q, k_cache, v_cache, out, T, start_pos, H, Hkv, D, window, scale, stream):
+    """prefill_attention on CPU tensors through pfa_prefill_attention_host."""
+    import ctypes
+    if out is None:
+        out = torch.empty(q.shape, dtype=q.dtype, pin_memory=q.is_pinned())
+    elif out.shape != q.shape or out.dtype != q.dtype or out.device.type != "cpu":
+        raise ValueError("out must match q in shape and dtype and be a CPU tensor")
+    for name, t in (("q", q), ("k_cache", k_cache), ("v_cache", v_cache), ("out", out)):
+        if not t.is_contiguous():
+            raise ValueError(f"{name} must be contiguous")
+    if T == 0:
+        return out
+    lib = _binding.load()
+    dev = torch.cuda.current_device()
+    dt = _DTYPES[q.dtype]
+    cuda_stream = stream if stream is not None else torch.cuda.current_stream(dev)
+    args = (q.data_ptr(), k_cache.data_ptr(), v_cache.data_ptr(), out.data_ptr(), int(T),
+            int(start_pos), int(H), int(Hkv), int(D), int(window), float(scale), dt)
+    with _host_lock:
+        buf = _host_bufs.get(dev)
+        rc = -2
+        if buf is not None:   # the kept buffer; PFA_ERR_SHAPE if it is too small
+            rc = lib.pfa_prefill_attention_host(*args, buf.data_ptr(), buf.numel(),
+                                                int(cuda_stream.cuda_stream))
+        if rc == -2:
+            n = ctypes.c_size_t(0)
+            rc = lib.pfa_host_buffer_bytes(int(T), int(start_pos), int(H), int(Hkv), int(D),
+                                           int(window), dt, ctypes.byref(n))
+            if rc != 0:
+                raise PfaError(rc, "pfa_host_buffer_bytes")
+            if buf is None or buf.numel() < n.value:
+                _host_bufs.pop(dev, None)
+                buf = torch.empty(int(n.value), dtype=torch.uint8,
+                                  device=torch.device("cuda", dev))
+                _host_bufs[dev] = buf
+            rc = lib.pfa_prefill_attention_host(*args, buf.data_ptr(), buf.numel(),
+                                                int(cuda_stream.cuda_stream))
+        if rc != 0:
+            raise PfaError(rc, "pfa_prefill_attention_host")
+        # out is read by the caller on return, and buf is free for the next call
+        cuda_stream.synchronize()
+    return out
 
 
 def prefill_attention_cache(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor,

@@ -25,6 +25,7 @@ STATUS = {
 EXPORTS = ("pfa_prefill_attention", "pfa_prefill_attention_ws", "pfa_workspace_bytes",
            "pfa_prefill_attention_noalloc", "pfa_prefill_attention_cache",
            "pfa_prefill_attention_graph", "pfa_schedule",
+           "pfa_prefill_attention_host", "pfa_host_buffer_bytes",
            "pfa_status_string",
            "pfa_last_device_error", "pfa_version", "pfa_debug_configure",
            "pfa_debug_check_schedule")
@@ -78,6 +79,12 @@ def load(path: str | None = None) -> ctypes.CDLL:
         lib.pfa_prefill_attention_graph.argtypes = [vp, vp, vp, vp, vp, i64, i32, i32, i32,
                                                     i32, ctypes.c_float, i32, i64, i64, i32, vp]
         lib.pfa_prefill_attention_graph.restype = i32
+        lib.pfa_prefill_attention_host.argtypes = [vp, vp, vp, vp, i64, i64, i32, i32, i32,
+                                                   i32, ctypes.c_float, i32, vp, sz, vp]
+        lib.pfa_prefill_attention_host.restype = i32
+        lib.pfa_host_buffer_bytes.argtypes = [i64, i64, i32, i32, i32, i32, i32,
+                                              ctypes.POINTER(sz)]
+        lib.pfa_host_buffer_bytes.restype = i32
         lib.pfa_status_string.argtypes = [i32]
         lib.pfa_status_string.restype = ctypes.c_char_p
         lib.pfa_last_device_error.argtypes = [vp]

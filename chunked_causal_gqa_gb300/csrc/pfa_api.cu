@@ -236,11 +236,11 @@ int prepare(const void* q, const void* k_cache, const void* v_cache, void* out, 
                         check_pointers, c);
 }
 
-int prepare_layout(const void* q, const void* k_cache, const void* v_cache, void* out,
-                   int64_t T, int64_t start_pos, int num_heads, int num_kv_heads, int head_dim,
-                   int window, float scale, int dtype, int64_t qkv_dim, int64_t max_seq_len,
-                   int ring, void* stream, bool check_pointers, Call* c) {
-  // ---- pure argument checks (no CUDA calls)
+// The argument checks of prepare_layout that need no pointer and no CUDA
+// call.  T == 0 passes once dtype, shape and scale do.
+int check_args(int64_t T, int64_t start_pos, int num_heads, int num_kv_heads, int head_dim,
+               int window, float scale, int dtype, int64_t qkv_dim, int64_t max_seq_len,
+               int ring) {
   if (dtype != PFA_F32 && dtype != PFA_BF16) return PFA_ERR_DTYPE;
   if (T < 0 || start_pos < 0 || num_heads <= 0 || num_kv_heads <= 0) return PFA_ERR_SHAPE;
   if (num_heads % num_kv_heads != 0) return PFA_ERR_SHAPE;
@@ -255,7 +255,6 @@ int prepare_layout(const void* q, const void* k_cache, const void* v_cache, void
   // TMA coordinates and launch indices are 32-bit.
   if (L > ((int64_t)1 << 31) - 4096 || T > ((int64_t)1 << 31) - 4096) return PFA_ERR_SHAPE;
   if (!std::isfinite(scale)) return PFA_ERR_VALUE;
-  c->T = T;
   if (T == 0) return PFA_OK;
   // ---- layout
   if (qkv_dim < (int64_t)num_heads * head_dim || max_seq_len <= 0 ||
@@ -271,6 +270,19 @@ int prepare_layout(const void* q, const void* k_cache, const void* v_cache, void
     if (dtype == PFA_BF16 && max_seq_len < L && max_seq_len % 128 != 0) return PFA_ERR_SHAPE;
   }
   if ((qkv_dim * (dtype == PFA_F32 ? 4 : 2)) % 16 != 0) return PFA_ERR_ALIGNMENT;
+  return PFA_OK;
+}
+
+int prepare_layout(const void* q, const void* k_cache, const void* v_cache, void* out,
+                   int64_t T, int64_t start_pos, int num_heads, int num_kv_heads, int head_dim,
+                   int window, float scale, int dtype, int64_t qkv_dim, int64_t max_seq_len,
+                   int ring, void* stream, bool check_pointers, Call* c) {
+  // ---- pure argument checks (no CUDA calls)
+  const int ac = check_args(T, start_pos, num_heads, num_kv_heads, head_dim, window, scale,
+                            dtype, qkv_dim, max_seq_len, ring);
+  if (ac != PFA_OK) return ac;
+  c->T = T;
+  if (T == 0) return PFA_OK;
   if (check_pointers) {
     if (!q || !k_cache || !v_cache || !out) return PFA_ERR_NULL;
     const uintptr_t mis = reinterpret_cast<uintptr_t>(q) | reinterpret_cast<uintptr_t>(k_cache) |
@@ -356,6 +368,75 @@ int dispatch(const Call& c, int dtype) {
                  c.ws_bytes, rc);
   return rc;
 }
+
+// ------------------------------------------------------------------ host-buffer entry
+namespace {
+
+constexpr int kHostGroups = 4;  // most kv-head groups of pfa_prefill_attention_host
+
+// Groups for a call moving `bytes` between host and device: one below 4 MiB
+// (the copies are too short to overlap), two below 128 MiB, else four --
+// the fastest of 1, 2 and 4 measured on GB300 for a 1.3 MB fp32 layer, the
+// 28 MB Mistral-shaped layer, the 46-67 MB head_dim-512 layers and the
+// 294 MB 64k chunk.
+int host_groups(size_t bytes, int num_kv_heads) {
+  const int g = bytes < ((size_t)4 << 20) ? 1 : (bytes < ((size_t)128 << 20) ? 2 : kHostGroups);
+  return std::min(g, num_kv_heads);
+}
+
+// Streams and events of the host-buffer entry on one device, created on the
+// first call there and kept until the process exits.
+struct HostPipe {
+  cudaStream_t s[kHostGroups];
+  cudaEvent_t fork;                  // the caller's stream reached the call
+  cudaEvent_t in_done[kHostGroups];  // group g's inputs are on the device
+  cudaEvent_t done[kHostGroups];     // group g's output is back in host memory
+};
+std::mutex g_host_mutex;  // held while a call enqueues its work
+HostPipe* g_host_pipe[64];
+
+int host_pipe(int dev, HostPipe** out) {
+  if (dev < 0 || dev >= 64) return kErrDevice;
+  if (!g_host_pipe[dev]) {
+    HostPipe hp;
+    bool ok = cudaEventCreateWithFlags(&hp.fork, cudaEventDisableTiming) == cudaSuccess;
+    for (int g = 0; g < kHostGroups && ok; ++g)
+      ok = cudaStreamCreateWithFlags(&hp.s[g], cudaStreamNonBlocking) == cudaSuccess &&
+           cudaEventCreateWithFlags(&hp.in_done[g], cudaEventDisableTiming) == cudaSuccess &&
+           cudaEventCreateWithFlags(&hp.done[g], cudaEventDisableTiming) == cudaSuccess;
+    if (!ok) {
+      cudaGetLastError();
+      return kErrDevice;
+    }
+    g_host_pipe[dev] = new HostPipe(hp);
+  }
+  *out = g_host_pipe[dev];
+  return kOk;
+}
+
+size_t round256(size_t x) { return (x + 255) & ~(size_t)255; }
+
+// Offsets of the device copies in the host entry's device buffer: q, k, v,
+// out; off[4] is the total size.
+void host_buffer_layout(int64_t T, int64_t L, int H, int Hkv, int D, int dtype, size_t off[5]) {
+  const size_t es = dtype == PFA_F32 ? 4 : 2;
+  const size_t qo = (size_t)T * H * D * es, kv = (size_t)Hkv * L * D * es;
+  off[0] = 0;
+  off[1] = round256(qo);
+  off[2] = off[1] + round256(kv);
+  off[3] = off[2] + round256(kv);
+  off[4] = off[3] + round256(qo);
+}
+
+// A T x width-byte block of rows `pitch` bytes apart (one copy when the rows
+// are contiguous).
+cudaError_t copy_rows(void* dst, const void* src, size_t pitch, size_t width, int64_t T,
+                      cudaStream_t s) {
+  if (width == pitch) return cudaMemcpyAsync(dst, src, (size_t)T * pitch, cudaMemcpyDefault, s);
+  return cudaMemcpy2DAsync(dst, pitch, src, pitch, width, (size_t)T, cudaMemcpyDefault, s);
+}
+
+}  // namespace
 
 }  // namespace pfa
 
@@ -469,6 +550,116 @@ int pfa_debug_check_schedule(int64_t T, int64_t start_pos, int num_heads, int nu
   c.max_seq_len = L;
   *failed_check = check_schedule_bf16_d128(c, num_sms, schedule, ctas);
   return PFA_OK;
+}
+
+int pfa_host_buffer_bytes(int64_t T, int64_t start_pos, int num_heads, int num_kv_heads,
+                          int head_dim, int window, int dtype, size_t* bytes) {
+  if (!bytes) return PFA_ERR_NULL;
+  *bytes = 0;
+  // a size computation: argument checks only, no device needed
+  const int rc = check_args(T, start_pos, num_heads, num_kv_heads, head_dim, window, 1.0f, dtype,
+                            (int64_t)num_heads * head_dim, start_pos + T, 0);
+  if (rc != PFA_OK || T == 0) return rc;
+  size_t off[5];
+  host_buffer_layout(T, start_pos + T, num_heads, num_kv_heads, head_dim, dtype, off);
+  *bytes = off[4];
+  return PFA_OK;
+}
+
+int pfa_prefill_attention_host(const void* q, const void* k_cache, const void* v_cache,
+                               void* out, int64_t T, int64_t start_pos, int num_heads,
+                               int num_kv_heads, int head_dim, int window, float scale,
+                               int dtype, void* device_buffer, size_t device_buffer_bytes,
+                               void* stream) {
+  // argument checks before any CUDA call, in the order of pfa_prefill_attention
+  const int64_t L = start_pos + T;
+  int rc = check_args(T, start_pos, num_heads, num_kv_heads, head_dim, window, scale, dtype,
+                      (int64_t)num_heads * head_dim, L, 0);
+  if (rc != PFA_OK || T == 0) return rc;
+  if (!q || !k_cache || !v_cache || !out || !device_buffer) return PFA_ERR_NULL;
+  if ((reinterpret_cast<uintptr_t>(q) | reinterpret_cast<uintptr_t>(k_cache) |
+       reinterpret_cast<uintptr_t>(v_cache) | reinterpret_cast<uintptr_t>(out)) & 15u)
+    return PFA_ERR_ALIGNMENT;
+  if (reinterpret_cast<uintptr_t>(device_buffer) & 255u) return PFA_ERR_ALIGNMENT;
+  size_t off[5];
+  host_buffer_layout(T, L, num_heads, num_kv_heads, head_dim, dtype, off);
+  if (device_buffer_bytes < off[4]) return PFA_ERR_SHAPE;
+  const size_t es = dtype == PFA_F32 ? 4 : 2;
+  const size_t row = (size_t)num_heads * head_dim * es;     // a token's q / out row
+  const size_t head_kv = (size_t)L * head_dim * es;         // a kv head's K (or V) block
+  const size_t qo = (size_t)T * row, kv = (size_t)num_kv_heads * head_kv;
+  if (overlaps(out, qo, q, qo) || overlaps(out, qo, k_cache, kv) ||
+      overlaps(out, qo, v_cache, kv) || overlaps(device_buffer, off[4], q, qo) ||
+      overlaps(device_buffer, off[4], k_cache, kv) || overlaps(device_buffer, off[4], v_cache, kv) ||
+      overlaps(device_buffer, off[4], out, qo))
+    return PFA_ERR_ALIAS;
+  // device checks
+  Call c0;
+  rc = prepare(nullptr, nullptr, nullptr, nullptr, T, start_pos, num_heads, num_kv_heads,
+               head_dim, window, scale, dtype, stream, false, &c0);
+  if (rc != PFA_OK) return rc;
+  if (!device_accessible(device_buffer, c0.device)) return PFA_ERR_DEVICE;
+
+  // One call per group of kv heads on the device copies: q / out rows keep
+  // the full row pitch (qkv_dim = H * D), K / V point at the group's heads.
+  char* base = static_cast<char*>(device_buffer);
+  char *qd = base + off[0], *kd = base + off[1], *vd = base + off[2], *od = base + off[3];
+  const int group = num_heads / num_kv_heads;
+  const int G = host_groups(2 * qo + 2 * kv, num_kv_heads);
+  Call gc[kHostGroups];
+  size_t col[kHostGroups], width[kHostGroups], kvoff[kHostGroups], kvlen[kHostGroups];
+  for (int g = 0; g < G; ++g) {
+    const int a = g * num_kv_heads / G, b = (g + 1) * num_kv_heads / G;
+    col[g] = (size_t)a * group * head_dim * es;
+    width[g] = (size_t)(b - a) * group * head_dim * es;
+    kvoff[g] = (size_t)a * head_kv;
+    kvlen[g] = (size_t)(b - a) * head_kv;
+    // the group's pointers lie inside the device buffer checked above
+    rc = prepare_layout(qd + col[g], kd + kvoff[g], vd + kvoff[g], od + col[g], T, start_pos,
+                        (b - a) * group, b - a, head_dim, window, scale, dtype,
+                        (int64_t)num_heads * head_dim, L, 0, nullptr, false, &gc[g]);
+    if (rc != PFA_OK) return rc;
+  }
+
+  std::lock_guard<std::mutex> lk(g_host_mutex);
+  HostPipe* hp = nullptr;
+  if ((rc = host_pipe(c0.device, &hp)) != kOk) return rc;
+  cudaStream_t user = static_cast<cudaStream_t>(stream);
+  if (cudaEventRecord(hp->fork, user) != cudaSuccess) {
+    cudaGetLastError();
+    return PFA_ERR_LAUNCH;
+  }
+  int status = PFA_OK;
+  int joined = 0;  // groups whose work `stream` must wait for
+  for (int g = 0; g < G && status == PFA_OK; ++g) {
+    cudaStream_t s = hp->s[g];
+    bool ok = cudaStreamWaitEvent(s, hp->fork, 0) == cudaSuccess &&
+              (g == 0 || cudaStreamWaitEvent(s, hp->in_done[g - 1], 0) == cudaSuccess);
+    // inputs: the group's K and V blocks and its q columns, groups in order
+    ok = ok &&
+         cudaMemcpyAsync(kd + kvoff[g], static_cast<const char*>(k_cache) + kvoff[g], kvlen[g],
+                         cudaMemcpyDefault, s) == cudaSuccess &&
+         cudaMemcpyAsync(vd + kvoff[g], static_cast<const char*>(v_cache) + kvoff[g], kvlen[g],
+                         cudaMemcpyDefault, s) == cudaSuccess &&
+         copy_rows(qd + col[g], static_cast<const char*>(q) + col[g], row, width[g], T, s) ==
+             cudaSuccess &&
+         cudaEventRecord(hp->in_done[g], s) == cudaSuccess;
+    if (ok) {
+      gc[g].stream = s;
+      status = dispatch(gc[g], dtype);
+      ok = status == PFA_OK &&
+           copy_rows(static_cast<char*>(out) + col[g], od + col[g], row, width[g], T, s) ==
+               cudaSuccess;
+    }
+    // whatever was queued on s is joined back into the caller's stream
+    if (cudaEventRecord(hp->done[g], s) == cudaSuccess) joined = g + 1;
+    if (!ok && status == PFA_OK) status = PFA_ERR_LAUNCH;
+  }
+  for (int g = 0; g < joined; ++g)
+    if (cudaStreamWaitEvent(user, hp->done[g], 0) != cudaSuccess && status == PFA_OK)
+      status = PFA_ERR_LAUNCH;
+  if (status != PFA_OK) cudaGetLastError();
+  return status;
 }
 
 int pfa_last_device_error(void* stream) {

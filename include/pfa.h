@@ -261,6 +261,69 @@ PFA_API int pfa_schedule(int64_t T, int64_t start_pos, int num_heads, int num_kv
                          size_t *workspace_bytes);
 
 /*
+ * pfa_host_buffer_bytes -- bytes of device memory pfa_prefill_attention_host
+ * needs for this shape (the device copies of q, k_cache, v_cache and out,
+ * each rounded up to 256 bytes).  The shape checks of
+ * pfa_prefill_attention; no device is needed and nothing is launched.
+ * Returns PFA_OK and sets *bytes (0 for T == 0), or an error status.
+ */
+PFA_API int pfa_host_buffer_bytes(int64_t T, int64_t start_pos, int num_heads, int num_kv_heads,
+                                  int head_dim, int window, int dtype, size_t *bytes);
+
+/*
+ * pfa_prefill_attention_host -- the operation of pfa_prefill_attention on
+ * HOST buffers: the batch buffers of the gnosis page "Prefill attention ->
+ * GPU: handoff" (section "GPU design", "Layout": q rows and the kv cache
+ * already populated on the host), copied to the device once per call into
+ * one caller-owned device buffer (section "Implementation status", open
+ * item 3: pool the device buffers instead of per-tile copies and
+ * allocations), with the copies overlapped with the attention kernels (the
+ * same page's "Expected ceiling" counts the per-layer host-device copies in
+ * the GPU time).
+ *
+ *   q, k_cache, v_cache  host, read only; the layouts of
+ *                        pfa_prefill_attention ([T][H][D], [Hkv][L][D]).
+ *   out                  host, [T][H][D]; written by a device-to-host copy
+ *                        that completes with the stream's work.
+ *   device_buffer        device memory on the current device, 256-byte
+ *                        aligned, of at least pfa_host_buffer_bytes(...)
+ *                        bytes (caller-owned; the call stores the device
+ *                        copies there).  Must not be in use by other work
+ *                        that can run at the same time.
+ *   device_buffer_bytes  its size.
+ *   other arguments      as for pfa_prefill_attention.
+ *
+ * Host buffers should be page-locked (cudaHostAlloc / cudaHostRegister) for
+ * the copies to be asynchronous and at full speed; pageable memory works,
+ * with copies the driver stages (partly synchronous to the host).
+ *
+ * Behaviour: asynchronous on `stream`; nothing is allocated.  The kv heads
+ * are processed in up to four groups (one when the call moves less than
+ * 4 MiB, two below 128 MiB, else four): each group's K/V rows and q columns
+ * are copied in (groups in order, so the first group's kernel starts while
+ * the later groups' data is still on its way), its kernel runs on its own
+ * copy of the group (plain schedule, as pfa_prefill_attention), and its
+ * out columns are copied back while later groups compute.  The groups run
+ * on streams of the library's own (created on the first call on a device,
+ * kept until the process exits) that wait for the work queued on `stream`
+ * before the call and that `stream` waits for in turn: synchronise `stream`
+ * (or wait for an event recorded on it after the call) before reading out.
+ * The result is bit-identical to pfa_prefill_attention on the same data.
+ *
+ * Errors: PFA_ERR_NULL for a null pointer, PFA_ERR_ALIGNMENT for a device
+ * buffer that is not 256-byte aligned or host buffers that are not 16-byte
+ * aligned, PFA_ERR_SHAPE for a device buffer smaller than required or the
+ * shape errors of pfa_prefill_attention, PFA_ERR_DEVICE when the device
+ * buffer is not device memory of the current device, PFA_ERR_LAUNCH when a
+ * copy or a launch is refused.  Nothing is enqueued on an argument error.
+ */
+PFA_API int pfa_prefill_attention_host(const void *q, const void *k_cache, const void *v_cache,
+                                       void *out, int64_t T, int64_t start_pos, int num_heads,
+                                       int num_kv_heads, int head_dim, int window, float scale,
+                                       int dtype, void *device_buffer, size_t device_buffer_bytes,
+                                       void *stream);
+
+/*
  * pfa_prefill_attention_noalloc -- the call of pfa_prefill_attention_ws with
  * the balanced schedule, for callers that cannot allocate device memory.
  * (The source pages have no counterpart: this is an interface convenience.)
