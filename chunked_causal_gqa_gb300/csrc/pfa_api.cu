@@ -416,16 +416,44 @@ int host_pipe(int dev, HostPipe** out) {
 
 size_t round256(size_t x) { return (x + 255) & ~(size_t)255; }
 
-// Offsets of the device copies in the host entry's device buffer: q, k, v,
-// out; off[4] is the total size.
-void host_buffer_layout(int64_t T, int64_t L, int H, int Hkv, int D, int dtype, size_t off[5]) {
+// The host entry's work split and device buffer for a prepared call c0 (the
+// contiguous layout): the device copies of q, k, v and out at off[0..3],
+// then one workspace per group of kv heads (the schedule
+// pfa_prefill_attention_ws picks for the group's heads alone; groups run
+// at the same time, so each has its own).
+struct HostPlan {
+  int G;                          // groups; group g has kv heads [a[g], a[g+1])
+  int a[kHostGroups + 1];
+  size_t off[4];
+  size_t ws_off[kHostGroups], ws_len[kHostGroups];
+  size_t total;                   // bytes of the device buffer
+};
+
+void host_plan(const Call& c0, int dtype, HostPlan* hp) {
   const size_t es = dtype == PFA_F32 ? 4 : 2;
-  const size_t qo = (size_t)T * H * D * es, kv = (size_t)Hkv * L * D * es;
-  off[0] = 0;
-  off[1] = round256(qo);
-  off[2] = off[1] + round256(kv);
-  off[3] = off[2] + round256(kv);
-  off[4] = off[3] + round256(qo);
+  const int64_t L = c0.start_pos + c0.T;
+  const size_t qo = (size_t)c0.T * c0.H * c0.D * es, kv = (size_t)c0.Hkv * L * c0.D * es;
+  hp->off[0] = 0;
+  hp->off[1] = round256(qo);
+  hp->off[2] = hp->off[1] + round256(kv);
+  hp->off[3] = hp->off[2] + round256(kv);
+  size_t at = hp->off[3] + round256(qo);
+  hp->G = host_groups(2 * qo + 2 * kv, c0.Hkv);
+  const int group = c0.H / c0.Hkv;
+  for (int g = 0; g <= hp->G; ++g) hp->a[g] = g * c0.Hkv / hp->G;
+  for (int g = 0; g < hp->G; ++g) {
+    size_t need = 0;
+    if (dtype == PFA_BF16 && c0.D == 128) {
+      Call cg = c0;
+      cg.Hkv = hp->a[g + 1] - hp->a[g];
+      cg.H = cg.Hkv * group;
+      need = workspace_bytes_bf16_d128(cg);
+    }
+    hp->ws_off[g] = at;
+    hp->ws_len[g] = need;
+    at += round256(need);
+  }
+  hp->total = at;
 }
 
 // A T x width-byte block of rows `pitch` bytes apart (one copy when the rows
@@ -556,13 +584,13 @@ int pfa_host_buffer_bytes(int64_t T, int64_t start_pos, int num_heads, int num_k
                           int head_dim, int window, int dtype, size_t* bytes) {
   if (!bytes) return PFA_ERR_NULL;
   *bytes = 0;
-  // a size computation: argument checks only, no device needed
-  const int rc = check_args(T, start_pos, num_heads, num_kv_heads, head_dim, window, 1.0f, dtype,
-                            (int64_t)num_heads * head_dim, start_pos + T, 0);
-  if (rc != PFA_OK || T == 0) return rc;
-  size_t off[5];
-  host_buffer_layout(T, start_pos + T, num_heads, num_kv_heads, head_dim, dtype, off);
-  *bytes = off[4];
+  Call c;
+  const int rc = prepare(nullptr, nullptr, nullptr, nullptr, T, start_pos, num_heads,
+                         num_kv_heads, head_dim, window, 1.0f, dtype, nullptr, false, &c);
+  if (rc != PFA_OK || c.T == 0) return rc;
+  HostPlan hp;
+  host_plan(c, dtype, &hp);
+  *bytes = hp.total;
   return PFA_OK;
 }
 
@@ -581,35 +609,37 @@ int pfa_prefill_attention_host(const void* q, const void* k_cache, const void* v
        reinterpret_cast<uintptr_t>(v_cache) | reinterpret_cast<uintptr_t>(out)) & 15u)
     return PFA_ERR_ALIGNMENT;
   if (reinterpret_cast<uintptr_t>(device_buffer) & 255u) return PFA_ERR_ALIGNMENT;
-  size_t off[5];
-  host_buffer_layout(T, L, num_heads, num_kv_heads, head_dim, dtype, off);
-  if (device_buffer_bytes < off[4]) return PFA_ERR_SHAPE;
   const size_t es = dtype == PFA_F32 ? 4 : 2;
   const size_t row = (size_t)num_heads * head_dim * es;     // a token's q / out row
   const size_t head_kv = (size_t)L * head_dim * es;         // a kv head's K (or V) block
   const size_t qo = (size_t)T * row, kv = (size_t)num_kv_heads * head_kv;
-  if (overlaps(out, qo, q, qo) || overlaps(out, qo, k_cache, kv) ||
-      overlaps(out, qo, v_cache, kv) || overlaps(device_buffer, off[4], q, qo) ||
-      overlaps(device_buffer, off[4], k_cache, kv) || overlaps(device_buffer, off[4], v_cache, kv) ||
-      overlaps(device_buffer, off[4], out, qo))
+  if (overlaps(out, qo, q, qo) || overlaps(out, qo, k_cache, kv) || overlaps(out, qo, v_cache, kv))
     return PFA_ERR_ALIAS;
-  // device checks
+  // device checks, then the split and the buffer it needs
   Call c0;
   rc = prepare(nullptr, nullptr, nullptr, nullptr, T, start_pos, num_heads, num_kv_heads,
                head_dim, window, scale, dtype, stream, false, &c0);
   if (rc != PFA_OK) return rc;
+  HostPlan plan;
+  host_plan(c0, dtype, &plan);
+  if (device_buffer_bytes < plan.total) return PFA_ERR_SHAPE;
+  if (overlaps(device_buffer, plan.total, q, qo) || overlaps(device_buffer, plan.total, k_cache, kv) ||
+      overlaps(device_buffer, plan.total, v_cache, kv) ||
+      overlaps(device_buffer, plan.total, out, qo))
+    return PFA_ERR_ALIAS;
   if (!device_accessible(device_buffer, c0.device)) return PFA_ERR_DEVICE;
 
   // One call per group of kv heads on the device copies: q / out rows keep
   // the full row pitch (qkv_dim = H * D), K / V point at the group's heads.
   char* base = static_cast<char*>(device_buffer);
-  char *qd = base + off[0], *kd = base + off[1], *vd = base + off[2], *od = base + off[3];
+  char *qd = base + plan.off[0], *kd = base + plan.off[1], *vd = base + plan.off[2],
+       *od = base + plan.off[3];
   const int group = num_heads / num_kv_heads;
-  const int G = host_groups(2 * qo + 2 * kv, num_kv_heads);
+  const int G = plan.G;
   Call gc[kHostGroups];
   size_t col[kHostGroups], width[kHostGroups], kvoff[kHostGroups], kvlen[kHostGroups];
   for (int g = 0; g < G; ++g) {
-    const int a = g * num_kv_heads / G, b = (g + 1) * num_kv_heads / G;
+    const int a = plan.a[g], b = plan.a[g + 1];
     col[g] = (size_t)a * group * head_dim * es;
     width[g] = (size_t)(b - a) * group * head_dim * es;
     kvoff[g] = (size_t)a * head_kv;
@@ -619,6 +649,10 @@ int pfa_prefill_attention_host(const void* q, const void* k_cache, const void* v
                         (b - a) * group, b - a, head_dim, window, scale, dtype,
                         (int64_t)num_heads * head_dim, L, 0, nullptr, false, &gc[g]);
     if (rc != PFA_OK) return rc;
+    if (plan.ws_len[g] > 0) {
+      gc[g].ws = base + plan.ws_off[g];
+      gc[g].ws_bytes = plan.ws_len[g];
+    }
   }
 
   std::lock_guard<std::mutex> lk(g_host_mutex);

@@ -262,10 +262,12 @@ PFA_API int pfa_schedule(int64_t T, int64_t start_pos, int num_heads, int num_kv
 
 /*
  * pfa_host_buffer_bytes -- bytes of device memory pfa_prefill_attention_host
- * needs for this shape (the device copies of q, k_cache, v_cache and out,
- * each rounded up to 256 bytes).  The shape checks of
- * pfa_prefill_attention; no device is needed and nothing is launched.
- * Returns PFA_OK and sets *bytes (0 for T == 0), or an error status.
+ * needs for this shape on the current device: the device copies of q,
+ * k_cache, v_cache and out, then one workspace per group of kv heads (bf16,
+ * head_dim 128: the size pfa_workspace_bytes gives for the group's heads
+ * alone), each rounded up to 256 bytes.  Same validation as
+ * pfa_workspace_bytes; nothing is launched.  Returns PFA_OK and sets *bytes
+ * (0 for T == 0), or an error status.
  */
 PFA_API int pfa_host_buffer_bytes(int64_t T, int64_t start_pos, int num_heads, int num_kv_heads,
                                   int head_dim, int window, int dtype, size_t *bytes);
@@ -302,13 +304,16 @@ PFA_API int pfa_host_buffer_bytes(int64_t T, int64_t start_pos, int num_heads, i
  * 4 MiB, two below 128 MiB, else four): each group's K/V rows and q columns
  * are copied in (groups in order, so the first group's kernel starts while
  * the later groups' data is still on its way), its kernel runs on its own
- * copy of the group (plain schedule, as pfa_prefill_attention), and its
+ * copy of the group (with the schedule pfa_prefill_attention_ws picks for
+ * the group's heads, in the group's workspace), and its
  * out columns are copied back while later groups compute.  The groups run
  * on streams of the library's own (created on the first call on a device,
  * kept until the process exits) that wait for the work queued on `stream`
  * before the call and that `stream` waits for in turn: synchronise `stream`
  * (or wait for an event recorded on it after the call) before reading out.
- * The result is bit-identical to pfa_prefill_attention on the same data.
+ * Each head's result is the one pfa_prefill_attention_ws computes for the
+ * group's heads alone: bit-identical to pfa_prefill_attention where the group
+ * runs the plain schedule, else equal within the split schedules' merge.
  *
  * Errors: PFA_ERR_NULL for a null pointer, PFA_ERR_ALIGNMENT for a device
  * buffer that is not 256-byte aligned or host buffers that are not 16-byte

@@ -90,16 +90,16 @@ def host_call(lib, q=A, k=B, v=C, o=O, T=16, sp=0, H=8, Hkv=2, D=128, w=0, scale
 
 
 def test_host_entry_validates_without_gpu(lib):
+    import torch
+    no_gpu = not torch.cuda.is_available()
     n = ctypes.c_size_t(7)
-    # sizes: q and out 16 x 8 x 128 bf16 = 32 KiB each, K and V 2 x 16 x 128 = 8 KiB each
-    assert lib.pfa_host_buffer_bytes(16, 0, 8, 2, 128, 0, BF16, ctypes.byref(n)) == 0
-    assert n.value == 2 * 32768 + 2 * 8192
-    assert lib.pfa_host_buffer_bytes(10, 5, 8, 2, 128, 0, F32, ctypes.byref(n)) == 0
-    assert n.value == 2 * 40960 + 2 * 15360            # 10x8x128x4 and 2x15x128x4, 256-aligned
     assert lib.pfa_host_buffer_bytes(16, 0, 6, 4, 128, 0, BF16, ctypes.byref(n)) == -2
     assert lib.pfa_host_buffer_bytes(16, 0, 8, 2, 128, 0, BF16, None) == -1
     assert lib.pfa_host_buffer_bytes(0, 0, 8, 2, 128, 0, BF16, ctypes.byref(n)) == 0
     assert n.value == 0
+    if no_gpu:   # the size depends on the device (its schedules)
+        assert lib.pfa_host_buffer_bytes(16, 0, 8, 2, 128, 0, BF16, ctypes.byref(n)) == -5
+    # checks that come before any CUDA call
     assert host_call(lib, dt=7) == -3
     assert host_call(lib, H=6, Hkv=4) == -2
     assert host_call(lib, scale=float("nan")) == -8
@@ -108,11 +108,8 @@ def test_host_entry_validates_without_gpu(lib):
     assert host_call(lib, buf=None) == -1
     assert host_call(lib, k=B + 8) == -4                 # host buffers: 16-byte aligned
     assert host_call(lib, buf=0x7000000000 + 16) == -4   # device buffer: 256-byte aligned
-    assert host_call(lib, nbuf=2 * 32768 + 2 * 8192 - 1) == -2   # device buffer too small
     assert host_call(lib, o=A + 64) == -9                # out overlaps q
-    assert host_call(lib, buf=B - 4096) == -9            # device buffer overlaps k_cache
-    import torch
-    if not torch.cuda.is_available():
+    if no_gpu:
         assert host_call(lib) == -5                      # valid arguments: the device check
 
 
