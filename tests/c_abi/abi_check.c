@@ -46,6 +46,19 @@ int main(void)
                                            &failed) == PFA_OK);
         CHECK(11, schedule == PFA_SCHEDULE_TAIL && failed == 0);
     }
+    {
+        /* the host-buffer entry: checks that need no device */
+        size_t bytes = 1;
+        void *dbuf = (void *)0x7000000000;
+        CHECK(12, pfa_host_buffer_bytes(16, 0, 6, 4, 128, 0, PFA_BF16, &bytes) == PFA_ERR_SHAPE);
+        CHECK(13, pfa_host_buffer_bytes(0, 0, 8, 2, 128, 0, PFA_BF16, &bytes) == PFA_OK &&
+                      bytes == 0);
+        CHECK(14, pfa_prefill_attention_host(q, k, v, out, 16, 0, 8, 2, 128, 0, 0.1f, PFA_BF16,
+                                             NULL, 1 << 20, NULL) == PFA_ERR_NULL);
+        CHECK(15, pfa_prefill_attention_host(q, k, v, out, 16, 0, 8, 2, 128, 0, 0.1f, PFA_BF16,
+                                             (char *)dbuf + 16, 1 << 20, NULL) ==
+                      PFA_ERR_ALIGNMENT);
+    }
     printf("abi_check: all checks passed\n");
     return 0;
 }
