@@ -127,3 +127,49 @@ def test_host_entry_rejects_bad_device_buffers():
     assert call(buf.data_ptr(), n) == 0
     torch.cuda.synchronize()
     assert pkg.last_device_error() == 0
+
+
+def test_host_entry_concurrent_callers():
+    """Two threads, each with its own stream and device buffer, call the C
+    entry back to back: every output equals the one a lone call gives."""
+    import threading
+    lib = _binding.load()
+    H, Hkv, D, T, sp = 16, 4, 128, 150, 2000
+    scale = 1.0 / D ** 0.5
+    n = _buffer_bytes(lib, T, sp, H, Hkv, D, _binding.PFA_BF16)
+    inputs = [tuple(x.pin_memory() for x in W.make_random(T, sp, H, Hkv, D, "bf16", seed=s,
+                                                          q_std=1.0, kv_std=0.5))
+              for s in (81, 82, 83, 84)]
+    want = [G.digest(pkg.prefill_attention(q, k, v, scale=scale)) for q, k, v in inputs]
+    errors = []
+
+    def worker(idx):
+        try:
+            s = torch.cuda.Stream()
+            buf = torch.empty(n, dtype=torch.uint8, device="cuda")
+            outs = []
+            for rep in range(6):
+                q, k, v = inputs[(idx + rep) % len(inputs)]
+                o = torch.empty((T, H, D), dtype=torch.bfloat16, pin_memory=True)
+                rc = lib.pfa_prefill_attention_host(q.data_ptr(), k.data_ptr(), v.data_ptr(),
+                                                    o.data_ptr(), T, sp, H, Hkv, D, 0, scale,
+                                                    _binding.PFA_BF16, buf.data_ptr(), n,
+                                                    s.cuda_stream)
+                if rc != 0:
+                    errors.append((idx, rep, rc))
+                    return
+                outs.append(((idx + rep) % len(inputs), o))
+            s.synchronize()
+            for which, o in outs:
+                if G.digest(o) != want[which]:
+                    errors.append((idx, which, "mismatch"))
+        except Exception as e:  # noqa: BLE001 -- reported below
+            errors.append((idx, repr(e)))
+
+    threads = [threading.Thread(target=worker, args=(i,)) for i in range(2)]
+    for t in threads:
+        t.start()
+    for t in threads:
+        t.join()
+    assert not errors, errors
+    assert pkg.last_device_error() == 0
