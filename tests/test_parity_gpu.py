@@ -33,7 +33,7 @@ BF16_CASES = [
     (8, 2, 128, 200, 0, 1000),     # window longer than the prompt
     (8, 2, 128, 1, 0, 0),          # a single first token
     (8, 2, 128, 1, 777, 0),        # a single token deep in the cache
-    # head_dim 512 (key tiles of 64, each CTA owning half of the output columns)
+    # head_dim 512 (key tiles of 128, each CTA owning half of the output columns)
     (8, 2, 512, 200, 100, 0),
     (8, 2, 512, 130, 0, 64),       # window of exactly one key tile
     (8, 2, 512, 150, 300, 1000),   # window longer than the visible prefix
