@@ -131,6 +131,13 @@ def test_python_binding_checks_tensors():
         pkg.prefill_attention(q, k[:, :3], k[:, :3])
     with pytest.raises(ValueError):
         pkg.prefill_attention(q[0], k, k)
+    # CPU tensors (the host-buffer path): layout checks before any device use
+    with pytest.raises(ValueError):
+        pkg.prefill_attention(q, k, k, out=torch.zeros(4, 8, 64, dtype=torch.bfloat16))
+    with pytest.raises(ValueError):
+        pkg.prefill_attention(q.transpose(0, 1).contiguous().transpose(0, 1), k, k)
+    assert pkg.prefill_attention(q[:0], k[:, :0], k[:, :0]).shape == (0, 8, 128)   # T = 0
+    pkg.release_host_buffers()   # nothing kept: a no-op
 
 
 def cache_call(lib, q=A, k=B, v=C, o=O, T=16, sp=100, H=8, Hkv=2, D=128, w=64, dt=BF16,
