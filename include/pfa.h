@@ -249,7 +249,9 @@ PFA_API int pfa_prefill_attention_graph(const void *q, const void *k_cache, cons
  *                          merge kernel (two launches);
  *   PFA_SCHEDULE_TAIL      the whole waves of pairs run whole and the pairs
  *                          of the last, partial wave are cut into equal key
- *                          ranges, then a merge kernel (two launches).
+ *                          ranges (with no more pairs than SMs: every pair
+ *                          is cut, the CTAs of one range running together),
+ *                          then a merge kernel (two launches).
  * Same validation as pfa_workspace_bytes; nothing is launched.  Returns
  * PFA_OK and sets both outputs, or an error status.
  */

@@ -207,8 +207,9 @@ def test_chunked_prefill_equals_one_shot(window):
     assert torch.allclose(chunk_b.float(), full_b[T1:].float(), atol=2e-2, rtol=1e-2)
 
 
-# Shapes where the balanced schedule is chosen: short chunks deep into the
-# cache (fewer query-tile pairs than SMs), with and without a window.
+# Shapes where a workspace schedule is chosen (the balanced table, or every
+# pair split into equal key ranges): short chunks deep into the cache (fewer
+# query-tile pairs than SMs), with and without a window.
 SCHEDULE_CASES = [
     (32, 8, 128, 128, 30000, 0),
     (8, 2, 128, 300, 20000, 0),
@@ -359,7 +360,7 @@ def test_softmax_dynamic_range(profile, D):
 def test_schedule_query_names_the_schedule_each_workload_gets():
     import chunked_causal_gqa_gb300 as pkg
     expect = {"mistral_1358": "plain", "chunk_64k": "tail", "chunk_128k": "tail",
-              "chunk_64k_t128": "balanced", "gemma_d512_global": "plain", "tiny_f32": "plain"}
+              "chunk_64k_t128": "tail", "gemma_d512_global": "plain", "tiny_f32": "plain"}
     for name, kind in expect.items():
         wl = W.WORKLOADS[name]
         got, nbytes = pkg.schedule(wl.T, wl.start_pos, wl.num_heads, wl.num_kv_heads,

@@ -51,7 +51,8 @@ def test_workloads_get_the_expected_schedules(lib):
     assert check(lib, 1358, 0, 32, 8, 0, 152)[:2] == (0, 176)      # Mistral layer: plain
     assert check(lib, 2048, 61440, 32, 8, 0, 152)[0] == 2          # 64k chunk: tail split
     assert check(lib, 2048, 129024, 32, 8, 0, 152)[0] == 2         # 128k chunk: tail split
-    assert check(lib, 128, 63360, 32, 8, 0, 152)[0] == 1           # short deep chunk: balanced
+    assert check(lib, 128, 63360, 32, 8, 0, 152)[:2] == (2, 144)   # short deep chunk: every pair split
+    assert check(lib, 1358, 0, 8, 2, 0, 152)[0] == 1               # few uneven pairs: balanced
 
 
 def test_arguments_are_checked(lib):
