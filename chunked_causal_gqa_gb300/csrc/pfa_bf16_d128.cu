@@ -20,7 +20,9 @@
 // (the log-sum-exp identity of the softmax; the result is deterministic):
 //   * tail split: with more pairs than SMs, the whole waves run whole and
 //     each pair of the last, partial wave is cut into equal key ranges, so
-//     the last wave fills the SMs (long chunks deep in a context);
+//     the last wave fills the SMs (long chunks deep in a context); with no
+//     more pairs than SMs, every pair is cut the same way in one wave (short
+//     chunks deep in a context: the CTAs of one range share its keys in L2);
 //   * balanced: the host cuts the pairs' key tiles into at most one run of
 //     items per SM, of equal cost (tiles plus a fixed per-item overhead) --
 //     chiefly short chunks deep into long contexts, where the plain schedule
