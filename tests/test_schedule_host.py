@@ -53,6 +53,10 @@ def test_workloads_get_the_expected_schedules(lib):
     assert check(lib, 2048, 129024, 32, 8, 0, 152)[0] == 2         # 128k chunk: tail split
     assert check(lib, 128, 63360, 32, 8, 0, 152)[:2] == (2, 144)   # short deep chunk: every pair split
     assert check(lib, 1358, 0, 8, 2, 0, 152)[0] == 1               # few uneven pairs: balanced
+    # every pair split, one wave: pairs x parts CTAs, at most one per SM
+    assert check(lib, 64, 1000, 8, 2, 0, 152)[:2] == (2, 18)       # 2 pairs x 9 ranges
+    kind, ctas, failed = check(lib, 128, 63360, 32, 8, 0, 100)
+    assert kind == 2 and ctas <= 100 and ctas % 16 == 0 and failed == 0
 
 
 def test_arguments_are_checked(lib):
