@@ -3,8 +3,9 @@
 One step = one call of the whole hot path (pfa_prefill_attention: QK^T, index
 mask, online softmax, PV, epilogue, all in the library's kernels) over one
 layer's chunk of synthetic, seeded inputs already resident in HBM.  The
-default workload is the Mistral-7B-shaped layer (32 query heads, 8 kv heads,
-head_dim 128, a 1358-token prompt, bf16); --workload selects another.
+default workload is the 128k-context chunk (32 query heads, 8 kv heads,
+head_dim 128, 2048 query tokens at start_pos 129024, so L = 131072, bf16):
+the largest configuration that one GPU holds; --workload selects another.
 
 Timing: W untimed warm-up steps; then K steps, each preceded (outside its
 timed span) by a 512 MiB write that flushes L2, each timed with CUDA events on
@@ -172,17 +173,22 @@ def oracle_rate_1thread(wl, max_rows: int = 2048):
     return flops / (time.perf_counter() - t0), len(rows)
 
 
-def oracle_sample(wl, budget_s: float):
+def oracle_sample(wl, budget_s: float, inputs=None):
     """Time the fp64 oracle on the host cores over a bounded sample of the
     workload's (token, head) rows.  Returns (flops/s, description, cores,
     seconds, rows, values): the rows timed and the oracle's outputs for them
-    (all rows in [T][H] order when the whole workload fits the budget)."""
+    (all rows in [T][H] order when the whole workload fits the budget).
+    `inputs` (q, k, v) may be passed to skip drawing them again."""
     import numpy as np
 
     import oracle
     from chunked_causal_gqa_gb300 import workloads as W
 
-    q, k, v = W.make_inputs(wl)
+    q, k, v = inputs if inputs is not None else W.make_inputs(wl)
+    # widen to float64 once, outside the timed calls (the oracle's own input
+    # format): the timing then covers the attention arithmetic only
+    q, k, v = (np.ascontiguousarray(x.double().numpy()) if hasattr(x, "double") else x
+               for x in (q, k, v))
     cores = oracle.default_threads()
     # estimate per-row cost from the visible key count; take evenly spaced rows
     T, H = wl.T, wl.num_heads
@@ -222,15 +228,48 @@ def _visible(wl, t):
     return min(pos + 1, wl.window) if wl.window > 0 else pos + 1
 
 
+def workload_config(wl, world: int) -> dict:
+    """The `config` object of the JSON line: the same for both arms."""
+    return {"workload": wl.name, "description": wl.description,
+            "num_heads": wl.num_heads, "num_kv_heads": wl.num_kv_heads,
+            "head_dim": wl.head_dim, "T": wl.T, "start_pos": wl.start_pos,
+            "window": wl.window, "seeds": list(wl.seeds),
+            "l2": "flushed before every timed step (512 MiB write)",
+            "parallelism": f"replicas x{world}"}
+
+
+def tolerance_report(got, want, dtype: str) -> dict:
+    """Errors of the GPU output against the oracle under both readings of the
+    bf16 bar: the allclose form |err| <= 2e-2 + 1e-2 |ref| (the one the tests
+    assert), and the stricter one in which |err| <= 2e-2 and |err| <= 1e-2 |ref|
+    must each hold.  fp32: max |err| <= 1e-4."""
+    import numpy as np
+    err = np.abs(got - want)
+    rep = {"elements": int(err.size), "max_abs_err": float(err.max()) if err.size else 0.0}
+    if dtype == "f32":
+        rep["bar"] = "max |err| <= 1e-4"
+        rep["ok"] = bool(rep["max_abs_err"] <= 1e-4)
+        return rep
+    ref = np.abs(want)
+    rep["bar"] = "|err| <= 2e-2 + 1e-2 |ref|"
+    rep["ok"] = bool(np.all(err <= 2e-2 + 1e-2 * ref))
+    rep["strict_abs_violations"] = int(np.count_nonzero(err > 2e-2))
+    rep["strict_rel_violations"] = int(np.count_nonzero(err > 1e-2 * ref))
+    rep["strict_ok"] = rep["strict_abs_violations"] == 0 and rep["strict_rel_violations"] == 0
+    return rep
+
+
 def run_reference(args, wl):
     rank, world, _ = dist_env()
     if rank != 0:
         return 0
+    from chunked_causal_gqa_gb300 import workloads as W
     times, descr, cores = [], "", 1
     budget = max(1.0, args.ref_seconds / max(1, args.steps + args.warmup))
     flops_s = []
+    inputs = tuple(x.double().numpy() for x in W.make_inputs(wl))
     for i in range(args.warmup + args.steps):
-        rate, descr, cores, dt, _, _ = oracle_sample(wl, budget)
+        rate, descr, cores, dt, _, _ = oracle_sample(wl, budget, inputs)
         if i >= args.warmup:
             flops_s.append(rate)
             times.append(dt)
@@ -240,7 +279,7 @@ def run_reference(args, wl):
         "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": 1e3 * statistics.mean(times), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": {"workload": wl.name, "description": wl.description},
+        "config": workload_config(wl, world),
         "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
                          "sample": descr},
         "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
@@ -388,7 +427,7 @@ def run_ours(args, wl):
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        rate, descr, cores, _, rows, vals = oracle_sample(wl, args.cpu_seconds)
+        rate, descr, cores, _, rows, vals = oracle_sample(wl, args.cpu_seconds, (q_h, k_h, v_h))
         cpu = {"value": rate / 1e12, "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
                "sample": descr}
         # the GPU output on the same rows against the oracle's values
@@ -396,6 +435,7 @@ def run_ours(args, wl):
         o = out.float().cpu().numpy().astype(np.float64)
         got = o[[t for t, _ in rows], [h for _, h in rows]]
         cpu["max_abs_err_vs_gpu"] = float(np.abs(got - vals).max())
+        cpu["tolerance_vs_gpu"] = tolerance_report(got, vals, wl.dtype)
         if wl.T * wl.num_heads <= 50000:   # the small configurations: also one thread
             r1, n1 = oracle_rate_1thread(wl)
             cpu["value_1thread"] = r1 / 1e12
@@ -407,12 +447,7 @@ def run_ours(args, wl):
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_step,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
             "dtype": wl.dtype, "data": "synthetic",
-            "config": {"workload": wl.name, "description": wl.description,
-                       "num_heads": wl.num_heads, "num_kv_heads": wl.num_kv_heads,
-                       "head_dim": wl.head_dim, "T": wl.T, "start_pos": wl.start_pos,
-                       "window": wl.window, "seeds": list(wl.seeds),
-                       "l2": "flushed before every timed step (512 MiB write)",
-                       "parallelism": f"replicas x{world}"},
+            "config": workload_config(wl, world),
             "prompt_tok_s_per_layer": world * wl.T / (ms_step * 1e-3),
             "frac_of_bf16_peak": value / world / float(peaks["bf16_tflops"]),
             "ms_min": min(per), "ms_median": statistics.median(per),
@@ -432,10 +467,10 @@ def run_ours(args, wl):
 def main(argv=None):
     ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=10000)
+    ap.add_argument("--steps", type=int, default=200)
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--workload", default="mistral_1358")
+    ap.add_argument("--workload", default="chunk_128k")
     ap.add_argument("--schedule", choices=["auto", "plain"], default="auto",
                     help="auto: the workspace schedule (tail split or balanced) where the "
                          "library picks one; plain: always one CTA per pair")

@@ -1060,11 +1060,13 @@ bool choose_schedule(const Shape& s, int sms, Plan* plan) {
   }
   {
     // preferred to the balanced table unless its estimate is over 15% longer
-    // (the estimate does not see the balanced table's second DRAM read)
+    // (the estimate does not see the balanced table's second DRAM read); any
+    // other choice it must beat outright
     std::unique_ptr<Plan> a(new Plan());
     int64_t m = 0;
+    const bool over_table = chosen && plan->sched.mode == kTable;
     if (plan_split_all(s, n, sms, a.get(), &m) && m < plain * 85 / 100 &&
-        (!chosen || m * 100 <= best * 115)) {
+        (!chosen || (over_table ? m * 100 <= best * 115 : m < best))) {
       *plan = *a;
       best = m;
       chosen = true;
@@ -1235,9 +1237,8 @@ int setup_kernel(const void* fn) {
 }
 
 int launch_bf16_d128(const Call& c) {
-  static int attr_state[64] = {0};  // 0: not checked, 1: ok, -1: unusable
-  if (c.device < 0 || c.device >= 64) return kErrDevice;
-  if (attr_state[c.device] == 0) {
+  static DeviceOnce setup;
+  const int sr = setup.run(c.device, [] {
     const void* fns[] = {
         (const void*)bf16_d128_kernel<true, false, SchedLite, false>,
         (const void*)bf16_d128_kernel<false, false, SchedLite, false>,
@@ -1247,14 +1248,11 @@ int launch_bf16_d128(const Call& c) {
         (const void*)bf16_d128_kernel<false, false, Sched, false>,
         (const void*)bf16_d128_kernel<true, true, SchedLite, false>,
         (const void*)bf16_d128_kernel<false, true, SchedLite, false>};
-    bool ok = true;
-    for (const void* fn : fns) ok = ok && setup_kernel(fn) == kOk;
-    attr_state[c.device] = ok ? 1 : -1;
-  }
-  if (attr_state[c.device] != 1) {
-    cudaGetLastError();
-    return kErrLaunch;
-  }
+    for (const void* fn : fns)
+      if (setup_kernel(fn) != kOk) return kErrLaunch;
+    return kOk;
+  });
+  if (sr != kOk) return sr;
   Shape s;
   if (!make_shape(c, &s)) return kErrShape;
 

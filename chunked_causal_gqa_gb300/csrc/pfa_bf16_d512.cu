@@ -432,21 +432,19 @@ bf16_d512_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
 }  // namespace
 
 int launch_bf16_d512(const Call& c) {
-  static int attr_done[64] = {0};
-  if (c.device < 0 || c.device >= 64) return kErrDevice;
-  if (!attr_done[c.device]) {
+  static DeviceOnce setup;
+  const int sr = setup.run(c.device, [] {
     const void* fns[4] = {(const void*)bf16_d512_kernel<true, false>,
                           (const void*)bf16_d512_kernel<false, false>,
                           (const void*)bf16_d512_kernel<true, true>,
                           (const void*)bf16_d512_kernel<false, true>};
     for (const void* fn : fns)
       if (cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemAlloc) !=
-          cudaSuccess) {
-        cudaGetLastError();
+          cudaSuccess)
         return kErrLaunch;
-      }
-    attr_done[c.device] = 1;
-  }
+    return kOk;
+  });
+  if (sr != kOk) return sr;
   const int group = c.H / c.Hkv;
   const int tok_per_tile = kBM / group;
   const int64_t tiles = (c.T + tok_per_tile - 1) / tok_per_tile;

@@ -199,14 +199,13 @@ size_t smem_bytes(int D) {
 }  // namespace
 
 int launch_f32(const Call& c) {
-  static int attr_done[64] = {0};
+  static DeviceOnce setup;
+  const int sr = setup.run(c.device, [] {
+    return cudaFuncSetAttribute(f32_attention_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                (int)smem_bytes(kMaxD)) == cudaSuccess ? kOk : kErrLaunch;
+  });
+  if (sr != kOk) return sr;
   const size_t smem = smem_bytes(c.D);
-  if (c.device >= 0 && c.device < 64 && !attr_done[c.device]) {
-    if (cudaFuncSetAttribute(f32_attention_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             (int)smem_bytes(kMaxD)) != cudaSuccess)
-      return kErrLaunch;
-    attr_done[c.device] = 1;
-  }
   F32Params p;
   p.q = static_cast<const float*>(c.q);
   p.k = static_cast<const float*>(c.k);

@@ -1,9 +1,11 @@
 // pfa_internal.h -- declarations shared by the C-ABI layer (pfa_api.cu) and
 // the kernel translation units.  Not part of the public interface.
 #pragma once
+#include <atomic>
 #include <cstdint>
 #include <cuda.h>
 #include <cuda_runtime.h>
+#include <mutex>
 
 namespace pfa {
 
@@ -53,6 +55,34 @@ constexpr int kFlagForceTimeout = 1;
 
 // Status codes (mirror pfa_status in include/pfa.h).
 constexpr int kOk = 0, kErrShape = -2, kErrDevice = -5, kErrLaunch = -6;
+
+// One-time set-up per device (a kernel's shared-memory opt-in), safe when
+// several host threads make their first call at the same time: the first
+// caller runs `f` under the lock, later callers read the recorded outcome.
+// Objects of this class have static storage duration (zero-initialised state).
+class DeviceOnce {
+ public:
+  template <class F>
+  int run(int device, F&& f) {
+    if (device < 0 || device >= kDevices) return kErrDevice;
+    int s = state_[device].load(std::memory_order_acquire);
+    if (s == 0) {
+      std::lock_guard<std::mutex> lk(mu_);
+      s = state_[device].load(std::memory_order_relaxed);
+      if (s == 0) {
+        s = (f() == kOk) ? 1 : -1;
+        if (s < 0) cudaGetLastError();  // clear the sticky-free error of the failed call
+        state_[device].store(s, std::memory_order_release);
+      }
+    }
+    return s > 0 ? kOk : kErrLaunch;
+  }
+
+ private:
+  static constexpr int kDevices = 64;
+  std::mutex mu_;
+  std::atomic<int> state_[kDevices];  // 0 not done, 1 ok, -1 failed
+};
 
 // Encodes a 3-D tiled bf16 tensor map (innermost dimension first).
 // Returns 0 on success.  Results are cached by all arguments.

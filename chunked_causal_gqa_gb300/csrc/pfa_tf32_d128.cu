@@ -443,17 +443,12 @@ __global__ void __launch_bounds__(kThreads, 1) tf32_d128_kernel(const Params p) 
 }  // namespace
 
 int launch_tf32_d128(const Call& c) {
-  static int attr_state[64] = {0};  // 0: not set, 1: ok, -1: unusable
-  if (c.device < 0 || c.device >= 64) return kErrDevice;
-  if (attr_state[c.device] == 0) {
-    attr_state[c.device] = cudaFuncSetAttribute(tf32_d128_kernel,
-                                                cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                                kSmemAlloc) == cudaSuccess ? 1 : -1;
-  }
-  if (attr_state[c.device] != 1) {
-    cudaGetLastError();
-    return kErrLaunch;
-  }
+  static DeviceOnce setup;
+  const int sr = setup.run(c.device, [] {
+    return cudaFuncSetAttribute(tf32_d128_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                kSmemAlloc) == cudaSuccess ? kOk : kErrLaunch;
+  });
+  if (sr != kOk) return sr;
   const int group = c.H / c.Hkv;
   const int tok_per_tile = kBM / group;
   const int64_t tiles = (c.T + tok_per_tile - 1) / tok_per_tile;

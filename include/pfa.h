@@ -352,7 +352,10 @@ PFA_API int pfa_prefill_attention_host(const void *q, const void *k_cache, const
  * PFA_ERR_SCRATCH before anything is launched (long chunks deep in a
  * context, whose tail split needs ~92 MiB for a 2048-token chunk of 32
  * heads, are refused; pfa_prefill_attention runs them with the plain
- * schedule).  Shapes that use no workspace (other dtypes or head_dims, or
+ * schedule).  It refuses rather than quietly running the plain schedule so
+ * that one promise holds: whenever it returns PFA_OK, its output is
+ * bit-identical to that of pfa_prefill_attention_ws given a large enough
+ * workspace.  Shapes that use no workspace (other dtypes or head_dims, or
  * shapes where the plain schedule is picked) run as pfa_prefill_attention.
  *
  * Sharing: every call on a device uses the same scratch and leaves its own

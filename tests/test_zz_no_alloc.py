@@ -5,8 +5,10 @@ It exists for callers that cannot allocate device memory around the call
 allocator): it runs the balanced schedule in the library's own static device
 scratch instead of a caller workspace.  These tests call it through the C ABI
 and compare it with the allocating entry point (pfa_prefill_attention_ws with
-a torch-allocated workspace), twice in a row on the same shared scratch, and
-check that a shape needing more than the static scratch is refused.
+a torch-allocated workspace), twice in a row on the same shared scratch:
+both entries run the same schedule, so the outputs must be bit-identical, and
+both must be within the bf16 bar of the fp64 oracle.  A shape needing more
+than the static scratch must be refused.
 """
 import ctypes
 
@@ -14,6 +16,7 @@ import pytest
 import torch
 
 import chunked_causal_gqa_gb300 as pkg
+import oracle
 from chunked_causal_gqa_gb300 import _binding
 from chunked_causal_gqa_gb300 import workloads as W
 from tests import gpu_util as G
@@ -52,12 +55,14 @@ def test_noalloc_matches_the_workspace_entry_on_two_calls_in_a_row(case):
     assert 0 < need <= SCRATCH_BYTES          # the shape runs in the static scratch
     ref = pkg.prefill_attention(q, k, v, window=w, scale=scale)   # caller workspace
     assert pkg.last_device_error() == 0
-    want = G.to_np(ref)
+    want = oracle.prefill_attention(q.cpu(), k.cpu(), v.cpu(), window=w, scale=scale)
+    G.check(G.to_np(ref), want, "bf16", "workspace entry vs oracle")
     for _ in range(2):
         out = torch.full_like(q, float("nan"))
         assert _call_noalloc(lib, q, k, v, out, sp, w, scale) == 0
         assert pkg.last_device_error() == 0
-        G.check(G.to_np(out), want, "bf16", "noalloc vs workspace entry")
+        assert torch.equal(out, ref), "noalloc and workspace entries differ in some bits"
+        G.check(G.to_np(out), want, "bf16", "noalloc vs oracle")
 
 
 def test_noalloc_refuses_a_shape_beyond_its_scratch():
