@@ -356,7 +356,7 @@ int dispatch(const Call& c, int dtype) {
   int rc;
   if (dtype == PFA_F32)
     // the tensor-core kernel packs a GQA group into 128-row tiles (group <= 128)
-    rc = (c.D == 128 && c.H / c.Hkv <= 128) ? launch_tf32_d128(c) : launch_f32(c);
+    rc = (c.D == 128 && c.H / c.Hkv <= 128) ? launch_f32x3_d128(c) : launch_f32(c);
   else if (c.D == 128)
     rc = launch_bf16_d128(c);
   else

@@ -105,7 +105,7 @@ int prepare_layout(const void* q, const void* k_cache, const void* v_cache, void
 int dispatch(const Call& c, int dtype);
 
 int launch_f32(const Call& c);       // fp32 on the CUDA cores, any head_dim
-int launch_tf32_d128(const Call& c); // fp32, head_dim 128, 3xTF32 on the tensor cores
+int launch_f32x3_d128(const Call& c); // fp32, head_dim 128, three bf16 products on the tensor cores
 int launch_bf16_d128(const Call& c);
 // Workspace bytes the head_dim-128 schedule the host picks needs (0: the plain
 // schedule); *schedule (if not null) gets 0 plain, 1 balanced, 2 tail split.

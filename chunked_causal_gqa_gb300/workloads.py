@@ -102,7 +102,7 @@ WORKLOADS = {
     "f32_chunk_16k": Workload(
         "f32_chunk_16k", 32, 8, 128, 2048, 14336, 0, "f32", 1.0, 0.5, (6000, 6001, 6002),
         "fp32 2048-token chunk at start_pos=14336 (L=16384): H=32, Hkv=8, D=128 "
-        "(the 3xTF32 tensor-core path at a size where it is not launch-bound)"),
+        "(the fp32 tensor-core path at a size where it is not launch-bound)"),
 }
 
 

@@ -33,8 +33,9 @@ BF16_CONST_REL = 2.0 ** -7
 BF16_MEAN_REL, BF16_MEAN_ABS = 2.0 ** -8, 2.0 ** -12
 
 # (H, Hkv, D, T, start_pos, window, dtype): both bf16 kernels, both fp32
-# kernels (3xTF32 for head_dim 128, CUDA cores otherwise), windows, a long
-# plain launch and shapes that take the workspace schedules.
+# kernels (three bf16 products on the tensor cores for head_dim 128, the CUDA
+# cores otherwise), windows, a long plain launch and shapes that take the
+# workspace schedules.
 CASES = [
     (32, 8, 128, 300, 200, 0, "bf16"),
     (8, 2, 128, 200, 9000, 0, "bf16"),      # long instance (71 key tiles per pair)
@@ -43,7 +44,7 @@ CASES = [
     (32, 8, 128, 1280, 2000, 0, "bf16"),    # tail split of the last pairs
     (8, 2, 512, 200, 100, 0, "bf16"),
     (8, 2, 512, 300, 700, 256, "bf16"),
-    (8, 2, 128, 300, 200, 0, "f32"),        # 3xTF32
+    (8, 2, 128, 300, 200, 0, "f32"),        # three bf16 products
     (8, 2, 128, 200, 500, 65, "f32"),
     (8, 2, 64, 150, 40, 0, "f32"),          # CUDA-core kernel
     (4, 2, 512, 40, 30, 7, "f32"),

@@ -24,7 +24,7 @@ CASES = [
     (6, 2, 128, 150, 20, 0, "bf16"),       # 1 group, group size 3
     (4, 1, 128, 77, 9, 0, "bf16"),         # 1 group, one kv head
     (8, 2, 512, 200, 100, 0, "bf16"),      # 4.3 MB: 2 groups of 1 kv head, head_dim 512
-    (8, 2, 128, 129, 0, 0, "f32"),         # 1 group, fp32 head_dim 128 (3xTF32)
+    (8, 2, 128, 129, 0, 0, "f32"),         # 1 group, fp32 head_dim 128 (bf16x3 tensor-core kernel)
     (8, 4, 64, 70, 30, 20, "f32"),         # 1 group, fp32 head_dim 64 (CUDA cores)
     (32, 8, 128, 300, 3000, 0, "bf16"),    # 18 MB: 2 groups of 4 kv heads
     (10, 5, 128, 130, 3000, 64, "bf16"),   # 8 MB: 2 uneven groups (2 + 3), window

@@ -62,7 +62,7 @@ F32_CASES = [
     (8, 2, 512, 33, 20, 0),
     (6, 3, 36, 40, 0, 5),
     (2, 2, 128, 1, 100, 0),
-    # head_dim 128: the 3xTF32 tensor-core kernel (key tiles of 64)
+    # head_dim 128: the tensor-core kernel (three bf16 products, key tiles of 128)
     (8, 2, 128, 300, 200, 0),      # GQA 4, ragged T and L
     (8, 2, 128, 129, 0, 0),        # one token past a tile, prompt from 0
     (4, 4, 128, 130, 5, 0),        # group 1: 128 tokens per tile
@@ -153,7 +153,7 @@ def test_large_config_full_output_parity(name, workspace):
 
 
 def test_f32_long_chunk_full_parity_and_bits():
-    """The 3xTF32 path at a size where it streams 16k keys per query tile:
+    """The fp32 tensor-core path at a size where it streams 16k keys per query tile:
     every output element against the whole oracle output, and bit-identical
     reruns."""
     wl = W.WORKLOADS["f32_chunk_16k"]
