@@ -443,11 +443,11 @@ void host_plan(const Call& c0, int dtype, HostPlan* hp) {
   for (int g = 0; g <= hp->G; ++g) hp->a[g] = g * c0.Hkv / hp->G;
   for (int g = 0; g < hp->G; ++g) {
     size_t need = 0;
-    if (dtype == PFA_BF16 && c0.D == 128) {
+    if (dtype == PFA_BF16) {
       Call cg = c0;
       cg.Hkv = hp->a[g + 1] - hp->a[g];
       cg.H = cg.Hkv * group;
-      need = workspace_bytes_bf16_d128(cg);
+      need = workspace_bytes_bf16(cg);
     }
     hp->ws_off[g] = at;
     hp->ws_len[g] = need;
@@ -534,7 +534,7 @@ int pfa_workspace_bytes(int64_t T, int64_t start_pos, int num_heads, int num_kv_
   const int rc = prepare(nullptr, nullptr, nullptr, nullptr, T, start_pos, num_heads,
                          num_kv_heads, head_dim, window, 1.0f, dtype, nullptr, false, &c);
   if (rc != PFA_OK || c.T == 0) return rc;
-  if (dtype == PFA_BF16 && head_dim == 128) *bytes = workspace_bytes_bf16_d128(c);
+  if (dtype == PFA_BF16) *bytes = workspace_bytes_bf16(c);
   return PFA_OK;
 }
 
@@ -547,8 +547,7 @@ int pfa_schedule(int64_t T, int64_t start_pos, int num_heads, int num_kv_heads, 
   const int rc = prepare(nullptr, nullptr, nullptr, nullptr, T, start_pos, num_heads,
                          num_kv_heads, head_dim, window, 1.0f, dtype, nullptr, false, &c);
   if (rc != PFA_OK || c.T == 0) return rc;
-  if (dtype == PFA_BF16 && head_dim == 128)
-    *workspace_bytes = workspace_bytes_bf16_d128(c, schedule);
+  if (dtype == PFA_BF16) *workspace_bytes = workspace_bytes_bf16(c, schedule);
   return PFA_OK;
 }
 

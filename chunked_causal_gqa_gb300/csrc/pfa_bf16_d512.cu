@@ -39,7 +39,11 @@
 
 #include <cuda_bf16.h>
 
+#include <algorithm>
+#include <climits>
 #include <cmath>
+#include <cstdint>
+#include <vector>
 
 namespace pfa {
 namespace {
@@ -75,8 +79,19 @@ constexpr uint32_t kColS = 0, kColO = 256;
 constexpr uint32_t kIdescQK = idesc_bf16_f32(kBM, kBN, false);
 constexpr uint32_t kIdescPV = idesc_bf16_f32(kBM, kDHalf, true);
 
+// Tail split (with a caller workspace): the whole waves of units run whole;
+// each unit of the last, partial wave is cut into `parts` equal key ranges
+// run as separate CTA pairs, part by part; a piece writes its unnormalised
+// output half, exponent base and row sum to a workspace slot, and
+// merge512_kernel combines the pieces of each unit in key order.
+constexpr int kPlainMode = 0, kTailMode = 2;
+constexpr size_t kOHalfFloats = (size_t)kBM * kDHalf;                 // one CTA's O, [col/4][row][4]
+constexpr size_t kSlotFloats512 = 2 * kOHalfFloats + 2 * 2 * kBM;    // O halves, base[2][128], sum[2][128]
+
 struct Params {
   __nv_bfloat16* out;
+  float* ws;         // tail split: the pieces' slots; else null
+  int mode, p1, p2, parts;
   int64_t o_stride;  // elements from one token's output row to the next
   int ring_rows;     // > 0: key j is in cache row j % ring_rows; 0: in row j
   int64_t T, start_pos;          // graph entry: T = the largest T, start_pos unused
@@ -120,9 +135,18 @@ bf16_d512_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
     if ((int)(blockIdx.x >> 1) >= tiles_per_head * p.Hkv) return;  // nothing set up yet
   }
 
-  // work unit: (d-half, kv head, query tile); latest tokens first
+  // CTA pair b (CTAs 2b and 2b+1, one per output half dh) runs unit b whole,
+  // or, past the whole waves of a tail split, part r of unit p1 + e.
+  // Unit: (kv head, query tile); latest tokens first.
   const int dh = blockIdx.x & 1;
-  const int rest = blockIdx.x >> 1;
+  const int pidx = blockIdx.x >> 1;
+  int rest = pidx, part = 0, slot = -1;
+  if (p.mode == kTailMode && pidx >= p.p1) {
+    const int j = pidx - p.p1;
+    part = j / p.p2;
+    rest = p.p1 + j % p.p2;
+    slot = j;
+  }
   const int kh = rest % p.Hkv;
   const int tile = tiles_per_head - 1 - rest / p.Hkv;
   const int64_t t0 = (int64_t)tile * p.tok_per_tile;
@@ -130,8 +154,11 @@ bf16_d512_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
   const int64_t pos_first = start_pos + t0;
   const int64_t pos_last = start_pos + t0 + p.tok_per_tile - 1;
   const int64_t kmin = p.window > 0 ? max((int64_t)0, pos_first - p.window + 1) : 0;
-  const int64_t kt_first = kmin / kBN;
-  const int n = (int)((start_pos + t_end - 1) / kBN - kt_first + 1);
+  const int n_unit = (int)((start_pos + t_end - 1) / kBN - kmin / kBN + 1);
+  const int kb = slot < 0 ? 0 : (int)((int64_t)n_unit * part / p.parts);
+  const int ke = slot < 0 ? n_unit : (int)((int64_t)n_unit * (part + 1) / p.parts);
+  const int64_t kt_first = kmin / kBN + kb;  // first key tile of this CTA's range
+  const int n = ke - kb;
   auto key_row = [&](int64_t key) -> int {
     return (int)(p.ring_rows > 0 ? key % p.ring_rows : key);
   };
@@ -398,7 +425,25 @@ bf16_d512_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
       ok = mbar_wait(bar(kBarO), (uint32_t)(n - 1) & 1u, abort_flag, p.err, lim);
       ok = __all_sync(0xffffffffu, ok);
     }
-    if (ok) {
+    if (ok && slot >= 0) {
+      // piece of a split unit: unnormalised fp32 output half, base and sum
+      tc_fence_after();
+      float* ws = p.ws + (size_t)slot * kSlotFloats512;
+      float4* ocol = reinterpret_cast<float4*>(ws + (size_t)dh * kOHalfFloats) + row;
+#pragma unroll 1
+      for (int c0 = 0; c0 < kDHalf; c0 += 32) {
+        uint32_t o[32];
+        tmem_ld32(tO + c0, o);
+        tmem_wait_ld(o);
+#pragma unroll
+        for (int j = 0; j < 8; ++j)
+          ocol[(size_t)(c0 / 4 + j) * kBM] =
+              make_float4(__uint_as_float(o[4 * j]), __uint_as_float(o[4 * j + 1]),
+                          __uint_as_float(o[4 * j + 2]), __uint_as_float(o[4 * j + 3]));
+      }
+      ws[2 * kOHalfFloats + dh * 2 * kBM + row] = m_run;
+      ws[2 * kOHalfFloats + dh * 2 * kBM + kBM + row] = l;
+    } else if (ok) {
       tc_fence_after();
       const float inv = l > 0.f ? 1.f / l : 0.f;
       __nv_bfloat16* orow = p.out + (t * p.o_stride + h * (int64_t)512 + dh * kDHalf);
@@ -429,7 +474,153 @@ bf16_d512_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
   }
 }
 
+// Combines the pieces of each split unit in key order:
+// m = max_r m_r, O = sum_r 2^(m_r - m) O_r, l = sum_r 2^(m_r - m) l_r, out = O / l.
+// Block (e, g): unit p1 + e, output columns 16 g .. 16 g + 15; thread = row
+// (the pieces' [col/4][row][4] layout makes every load coalesced).
+constexpr int kMerge512Cols = 16;
+
+__global__ void __launch_bounds__(kBM) merge512_kernel(const Params p) {
+  const int e = blockIdx.x;
+  const int unit = p.p1 + e;
+  const int kh = unit % p.Hkv;
+  const int tile = p.tiles_per_head - 1 - unit / p.Hkv;
+  const int row = threadIdx.x;
+  const int tok = row / p.group;
+  const int64_t t = (int64_t)tile * p.tok_per_tile + tok;
+  if (tok >= p.tok_per_tile || t >= p.T) return;
+  const int h = kh * p.group + row % p.group;
+  const int col0 = blockIdx.y * kMerge512Cols;
+  const int dh = col0 / kDHalf;
+  const int cq0 = (col0 % kDHalf) / 4;  // first column quad within the half
+  auto slot = [&](int r) -> const float* {
+    return p.ws + (size_t)(r * p.p2 + e) * kSlotFloats512;
+  };
+  const size_t off_m = 2 * kOHalfFloats + (size_t)dh * 2 * kBM + row, off_l = off_m + kBM;
+  float m = -INFINITY;
+  for (int r = 0; r < p.parts; ++r) m = fmaxf(m, slot(r)[off_m]);
+  const float mb = (m == -INFINITY) ? 0.f : m;
+  float4 acc[kMerge512Cols / 4];
+#pragma unroll
+  for (int q = 0; q < kMerge512Cols / 4; ++q) acc[q] = make_float4(0.f, 0.f, 0.f, 0.f);
+  float l = 0.f;
+  for (int r = 0; r < p.parts; ++r) {
+    const float* ws = slot(r);
+    const float w = ex2(ws[off_m] - mb);  // 0 for a piece that saw no visible key
+    l = fmaf(w, ws[off_l], l);
+    const float4* ocol = reinterpret_cast<const float4*>(ws + (size_t)dh * kOHalfFloats) + row;
+#pragma unroll
+    for (int q = 0; q < kMerge512Cols / 4; ++q) {
+      const float4 o = ocol[(size_t)(cq0 + q) * kBM];
+      acc[q].x = fmaf(w, o.x, acc[q].x);
+      acc[q].y = fmaf(w, o.y, acc[q].y);
+      acc[q].z = fmaf(w, o.z, acc[q].z);
+      acc[q].w = fmaf(w, o.w, acc[q].w);
+    }
+  }
+  const float inv = l > 0.f ? 1.f / l : 0.f;
+  uint32_t wv[kMerge512Cols / 2];
+#pragma unroll
+  for (int q = 0; q < kMerge512Cols / 4; ++q) {
+    wv[2 * q] = pack_bf16x2(acc[q].x * inv, acc[q].y * inv);
+    wv[2 * q + 1] = pack_bf16x2(acc[q].z * inv, acc[q].w * inv);
+  }
+  uint4* dst = reinterpret_cast<uint4*>(p.out + t * p.o_stride + h * (int64_t)512 + col0);
+#pragma unroll
+  for (int q = 0; q < kMerge512Cols / 8; ++q)
+    dst[q] = make_uint4(wv[4 * q], wv[4 * q + 1], wv[4 * q + 2], wv[4 * q + 3]);
+}
+
+// ------------------------------------------------------------------ host
+// Schedule of one shape: plain, or the tail split.
+struct Plan512 {
+  int mode = kPlainMode, p1 = 0, p2 = 0, parts = 0;
+  size_t ws_bytes = 0;
+};
+
+// Key tiles of unit u, as the kernel derives them.
+int unit_tiles(const Call& c, int tiles_per_head, int tok_per_tile, int u) {
+  const int tile = tiles_per_head - 1 - u / c.Hkv;
+  const int64_t t0 = (int64_t)tile * tok_per_tile;
+  const int64_t t_end = std::min<int64_t>(t0 + tok_per_tile, c.T);
+  const int64_t pos_first = c.start_pos + t0;
+  const int64_t kmin = c.window > 0 ? std::max<int64_t>(0, pos_first - c.window + 1) : 0;
+  return (int)((c.start_pos + t_end - 1) / kBN - kmin / kBN + 1);
+}
+
+// Fixed cost of a CTA (Q load, pipeline fill, epilogue) and of the merge, in
+// key-tile units.
+constexpr int64_t kCtaOverheadTiles = 2, kMerge512CostTiles = 2;
+constexpr int kMaxParts512 = 8;
+
+// Makespan, in key-tile units, of CTAs launched in order on `sms` SMs (the
+// hardware starts each on the first SM that frees up).
+int64_t makespan(const std::vector<int64_t>& costs, int sms) {
+  std::vector<int64_t> free_at((size_t)std::max(sms, 1), 0);
+  int64_t end = 0;
+  for (int64_t cost : costs) {
+    std::pop_heap(free_at.begin(), free_at.end(), std::greater<int64_t>());
+    free_at.back() += cost;
+    end = std::max(end, free_at.back());
+    std::push_heap(free_at.begin(), free_at.end(), std::greater<int64_t>());
+  }
+  return end;
+}
+
+// The tail split is taken when it beats the plain schedule's estimate by 5%.
+Plan512 plan_d512(const Call& c) {
+  Plan512 plan;
+  if (c.lens != nullptr || c.num_sms < 2) return plan;
+  const int group = c.H / c.Hkv;
+  const int tok_per_tile = kBM / group;
+  const int64_t tiles = (c.T + tok_per_tile - 1) / tok_per_tile;
+  const int64_t U = tiles * c.Hkv;
+  const int per_wave = c.num_sms / 2;  // units (CTA pairs) per wave
+  if (U <= per_wave || U > (1 << 20)) return plan;
+  const int p1 = per_wave * (int)(U / per_wave), p2 = (int)(U - p1);
+  if (p2 == 0) return plan;
+  std::vector<int> n((size_t)U);
+  int nmin = INT32_MAX;
+  for (int u = 0; u < (int)U; ++u) {
+    n[u] = unit_tiles(c, (int)tiles, tok_per_tile, u);
+    if (u >= p1) nmin = std::min(nmin, n[u]);
+  }
+  std::vector<int64_t> costs;
+  for (int u = 0; u < (int)U; ++u)
+    for (int d = 0; d < 2; ++d) costs.push_back(n[u] + kCtaOverheadTiles);
+  const int64_t plain = makespan(costs, c.num_sms);
+  int64_t best = INT64_MAX;
+  for (int parts = 2; parts <= kMaxParts512 && parts <= nmin; ++parts) {
+    costs.clear();
+    for (int u = 0; u < p1; ++u)
+      for (int d = 0; d < 2; ++d) costs.push_back(n[u] + kCtaOverheadTiles);
+    for (int r = 0; r < parts; ++r)
+      for (int e = 0; e < p2; ++e) {
+        const int64_t nu = n[p1 + e];
+        for (int d = 0; d < 2; ++d)
+          costs.push_back(nu * (r + 1) / parts - nu * r / parts + kCtaOverheadTiles);
+      }
+    const int64_t m = makespan(costs, c.num_sms) + kMerge512CostTiles;
+    if (m < best) {
+      best = m;
+      plan.parts = parts;
+    }
+  }
+  if (plan.parts == 0 || best * 100 >= plain * 95) return Plan512{};
+  plan.mode = kTailMode;
+  plan.p1 = p1;
+  plan.p2 = p2;
+  plan.ws_bytes = (size_t)p2 * plan.parts * kSlotFloats512 * sizeof(float);
+  return plan;
+}
+
 }  // namespace
+
+size_t workspace_bytes_bf16_d512(const Call& c, int* schedule) {
+  const Plan512 plan = plan_d512(c);
+  if (schedule) *schedule = plan.mode == kTailMode ? 2 : 0;
+  return plan.ws_bytes;
+}
 
 int launch_bf16_d512(const Call& c) {
   static DeviceOnce setup;
@@ -467,8 +658,19 @@ int launch_bf16_d512(const Call& c) {
     if (encode_tmap_bf16_3d(&tk, c.k, dims, strides, kbox)) return kErrLaunch;
     if (encode_tmap_bf16_3d(&tv, c.v, dims, strides, vbox)) return kErrLaunch;
   }
+  // the tail split when the caller gave a large enough workspace
+  Plan512 plan;
+  if (c.ws != nullptr && c.lens == nullptr) {
+    plan = plan_d512(c);
+    if (plan.ws_bytes > c.ws_bytes) plan = Plan512{};
+  }
   Params p;
   p.out = static_cast<__nv_bfloat16*>(c.out);
+  p.ws = plan.mode == kTailMode ? static_cast<float*>(c.ws) : nullptr;
+  p.mode = plan.mode;
+  p.p1 = plan.p1;
+  p.p2 = plan.p2;
+  p.parts = plan.parts;
   p.o_stride = c.qkv_dim;
   p.ring_rows = ring_rows(c);
   p.T = c.T;
@@ -485,7 +687,10 @@ int launch_bf16_d512(const Call& c) {
   p.err = c.err;
   p.wait_limit_ns = c.wait_limit_ns;
   p.flags = c.flags;
-  const dim3 grid((unsigned)(2 * tiles * c.Hkv));
+  const int64_t pairs = plan.mode == kTailMode
+                            ? (int64_t)plan.p1 + (int64_t)plan.p2 * plan.parts
+                            : tiles * c.Hkv;
+  const dim3 grid((unsigned)(2 * pairs));
   const bool fold = p.scale_log2 > 0.f;
   if (c.lens) {
     if (fold)
@@ -497,7 +702,12 @@ int launch_bf16_d512(const Call& c) {
   } else {
     bf16_d512_kernel<false, false><<<grid, kThreads, kSmemAlloc, c.stream>>>(tq, tk, tv, p);
   }
-  return cudaGetLastError() == cudaSuccess ? kOk : kErrLaunch;
+  if (cudaGetLastError() != cudaSuccess) return kErrLaunch;
+  if (plan.mode == kTailMode) {
+    merge512_kernel<<<dim3((unsigned)plan.p2, 512 / kMerge512Cols), kBM, 0, c.stream>>>(p);
+    if (cudaGetLastError() != cudaSuccess) return kErrLaunch;
+  }
+  return kOk;
 }
 
 }  // namespace pfa

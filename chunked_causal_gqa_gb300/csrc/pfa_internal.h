@@ -111,6 +111,16 @@ int launch_bf16_d128(const Call& c);
 // schedule); *schedule (if not null) gets 0 plain, 1 balanced, 2 tail split.
 size_t workspace_bytes_bf16_d128(const Call& c, int* schedule = nullptr);
 int launch_bf16_d512(const Call& c);
+// Workspace bytes of the head_dim-512 schedule the host picks (0: plain);
+// *schedule (if not null) gets 0 plain or 2 tail split.
+size_t workspace_bytes_bf16_d512(const Call& c, int* schedule = nullptr);
+// Workspace bytes of the schedule a bf16 call gets (either head_dim).
+inline size_t workspace_bytes_bf16(const Call& c, int* schedule = nullptr) {
+  if (c.D == 128) return workspace_bytes_bf16_d128(c, schedule);
+  if (c.D == 512) return workspace_bytes_bf16_d512(c, schedule);
+  if (schedule) *schedule = 0;
+  return 0;
+}
 // Host-only replay of the head_dim-128 work assignment with its invariants
 // (pfa_debug_check_schedule); 0 or the number of the failed check.
 int check_schedule_bf16_d128(const Call& c, int sms, int* schedule, int* ctas);

@@ -117,7 +117,7 @@ PFA_API int pfa_prefill_attention(const void *q, const void *k_cache, const void
 
 /*
  * pfa_prefill_attention_ws -- pfa_prefill_attention with a caller-provided
- * device workspace that enables the balanced schedule.
+ * device workspace that enables the split-key schedules.
  *
  *   workspace        device pointer (256-byte aligned) or NULL, not
  *                    overlapping q, k_cache, v_cache or out.  Its contents on
@@ -134,7 +134,11 @@ PFA_API int pfa_prefill_attention(const void *q, const void *k_cache, const void
  * the workspace, which a second kernel on the same stream combines in a fixed
  * order.  The result is deterministic for a given device and shape, and equal
  * to the plain schedule's within floating-point reassociation (both are
- * within the stated tolerance of the exact result).  Concurrent calls must
+ * within the stated tolerance of the exact result).  For bf16 with head_dim
+ * 512 the workspace enables the tail split only (see pfa_schedule): the
+ * whole waves of query tiles run whole, and each tile of a last, partial
+ * wave is cut into equal key ranges whose partial results are combined in
+ * key order.  Concurrent calls must
  * not share a workspace.  Other arguments, ownership and errors: as for
  * pfa_prefill_attention (PFA_ERR_ALIGNMENT / PFA_ERR_DEVICE / PFA_ERR_ALIAS
  * also cover the workspace).
@@ -244,14 +248,19 @@ PFA_API int pfa_prefill_attention_graph(const void *q, const void *k_cache, cons
  * pfa_schedule -- which schedule pfa_prefill_attention_ws runs for this shape
  * on the current device when its workspace is at least *workspace_bytes
  * (the value pfa_workspace_bytes reports):
- *   PFA_SCHEDULE_PLAIN     one kernel, one CTA per pair of 128-row query tiles;
+ *   PFA_SCHEDULE_PLAIN     one kernel, one CTA per pair of 128-row query tiles
+ *                          (head_dim 512: two CTAs per query tile, one per
+ *                          half of the output columns);
  *   PFA_SCHEDULE_BALANCED  equal-cost runs of key-tile ranges per SM, then a
  *                          merge kernel (two launches);
  *   PFA_SCHEDULE_TAIL      the whole waves of pairs run whole and the pairs
  *                          of the last, partial wave are cut into equal key
  *                          ranges (with no more pairs than SMs: every pair
  *                          is cut, the CTAs of one range running together),
- *                          then a merge kernel (two launches).
+ *                          then a merge kernel (two launches).  head_dim 512
+ *                          has this schedule (with query tiles in place of
+ *                          pairs, and without the every-pair form) and the
+ *                          plain one; fp32 has the plain one only.
  * Same validation as pfa_workspace_bytes; nothing is launched.  Returns
  * PFA_OK and sets both outputs, or an error status.
  */
@@ -265,9 +274,9 @@ PFA_API int pfa_schedule(int64_t T, int64_t start_pos, int num_heads, int num_kv
 /*
  * pfa_host_buffer_bytes -- bytes of device memory pfa_prefill_attention_host
  * needs for this shape on the current device: the device copies of q,
- * k_cache, v_cache and out, then one workspace per group of kv heads (bf16,
- * head_dim 128: the size pfa_workspace_bytes gives for the group's heads
- * alone), each rounded up to 256 bytes.  Same validation as
+ * k_cache, v_cache and out, then one workspace per group of kv heads (bf16:
+ * the size pfa_workspace_bytes gives for the group's heads alone), each
+ * rounded up to 256 bytes.  Same validation as
  * pfa_workspace_bytes; nothing is launched.  Returns PFA_OK and sets *bytes
  * (0 for T == 0), or an error status.
  */

@@ -385,3 +385,34 @@ def test_tail_split_on_a_windowed_layer():
     plain = G.run(q, k, v, window=w, workspace=None)
     G.check(G.to_np(plain)[[t for t, _ in rows], [h for _, h in rows]], want, "bf16",
             "plain+window")
+
+
+# head_dim 512 with a last, partial wave of query tiles: the tail split cuts
+# each tile of that wave into equal key ranges (groups of 8 heads: 16 tokens
+# per tile; 80 or 82 tiles on 76 CTA pairs per wave).
+D512_TAIL_CASES = [
+    (16, 2, 512, 640, 4000, 0),
+    (16, 2, 512, 650, 4000, 0),      # ragged T
+    (16, 2, 512, 640, 4000, 1000),   # sliding window
+]
+
+
+@pytest.mark.parametrize("case", D512_TAIL_CASES, ids=lambda c: "H%d_Hkv%d_D%d_T%d_sp%d_w%d" % c)
+def test_d512_tail_split_agrees_with_oracle_and_plain(case):
+    import chunked_causal_gqa_gb300 as pkg
+    H, Hkv, D, T, sp, w = case
+    sched, need = pkg.schedule(T, sp, H, Hkv, D, w)
+    assert sched == "tail" and need > 0
+    q, k, v = W.make_random(T, sp, H, Hkv, D, "bf16", seed=sum(case) + 3, kv_std=0.5)
+    want = oracle.prefill_attention(q, k, v, window=w)
+    plain = G.run(q, k, v, window=w, workspace=None)
+    G.check(G.to_np(plain), want, "bf16", "plain " + str(case))
+    tail = G.run(q, k, v, window=w)
+    G.check(G.to_np(tail), want, "bf16", "tail " + str(case))
+    # an explicit workspace gives the same bits; one byte short falls back to
+    # plain; reruns are bit-identical
+    ws = torch.full((need,), 255, dtype=torch.uint8, device=G.dev())
+    assert torch.equal(G.run(q, k, v, window=w, workspace=ws), tail)
+    small = torch.empty(need - 1, dtype=torch.uint8, device=G.dev())
+    assert torch.equal(G.run(q, k, v, window=w, workspace=small), plain)
+    assert G.digest(G.run(q, k, v, window=w)) == G.digest(tail)
