@@ -20,7 +20,8 @@
 //
 // CTA = one kv head x one 128-row query tile (all `group` query heads of the
 // kv head for 128/group consecutive tokens; row r -> token r/group, head
-// r%group), latest tokens first.  Key tiles of 128.
+// r%group); CTAs in kv-head-major order, latest tokens first within a head.
+// Key tiles of 128.
 //
 // Warp roles (9 warps):
 //   warps 0-3  rows of the tile (TMEM lanes 0-127, one row per thread): split
@@ -167,9 +168,11 @@ __global__ void __launch_bounds__(kThreads, 1) f32x3_d128_kernel(const Params p)
     if ((int)blockIdx.x >= tiles_per_head * p.Hkv) return;  // nothing set up yet
   }
 
-  // work unit: (kv head, query tile); latest tokens first
-  const int kh = (int)blockIdx.x % p.Hkv;
-  const int tile = tiles_per_head - 1 - (int)blockIdx.x / p.Hkv;
+  // work unit: (kv head, query tile), kv head major, latest tokens first
+  // within a head: the CTAs in flight cover few kv heads, so the fp32 K/V
+  // they stream (16 MB per head at 16k keys) stays in L2 between them
+  const int kh = (int)blockIdx.x / tiles_per_head;
+  const int tile = tiles_per_head - 1 - (int)blockIdx.x % tiles_per_head;
   const int64_t t0 = (int64_t)tile * p.tok_per_tile;
   const int64_t t_end = min(t0 + p.tok_per_tile, T);
   const int64_t pos_first = start_pos + t0;
