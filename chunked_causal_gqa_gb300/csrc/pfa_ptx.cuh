@@ -253,36 +253,6 @@ __device__ __forceinline__ void mma4_ts(uint32_t d_tmem, uint32_t a_tmem, uint64
       : "memory");
 }
 
-// Instruction descriptor of kind::tf32 with tf32 A/B (both K-major), fp32 D.
-__host__ __device__ constexpr uint32_t idesc_tf32_f32(int M, int N) {
-  return (1u << 4)                       // D format: f32
-       | (2u << 7)                       // A format: tf32
-       | (2u << 10)                      // B format: tf32
-       | ((uint32_t)(N >> 3) << 17)      // N / 8
-       | ((uint32_t)(M >> 4) << 24);     // M / 16
-}
-
-// Four K=8 steps of D (+)= A * B, kind::tf32, A in tensor memory (columns
-// a_tmem + 8 kk, one tf32 per column) and B K-major in shared memory within
-// one 128-byte swizzle span (descriptor b0 + 2 kk: 32 bytes per step).  The
-// first step accumulates iff `accumulate`; the rest always accumulate.
-__device__ __forceinline__ void mma4_tf32_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b0,
-                                             uint32_t idesc, uint32_t accumulate) {
-  asm volatile(
-      "{\n\t.reg .pred e, acc;\n\t.reg .b64 b;\n\t.reg .b32 a;\n\t"
-      "elect.sync _|e, 0xffffffff;\n\t"
-      "setp.ne.b32 acc, %4, 0;\n\t"
-      "@e tcgen05.mma.cta_group::1.kind::tf32 [%0], [%1], %2, %3, acc;\n\t"
-      "add.s32 a, %1, 8;  add.s64 b, %2, 2;\n\t"
-      "@e tcgen05.mma.cta_group::1.kind::tf32 [%0], [a], b, %3, e;\n\t"
-      "add.s32 a, %1, 16; add.s64 b, %2, 4;\n\t"
-      "@e tcgen05.mma.cta_group::1.kind::tf32 [%0], [a], b, %3, e;\n\t"
-      "add.s32 a, %1, 24; add.s64 b, %2, 6;\n\t"
-      "@e tcgen05.mma.cta_group::1.kind::tf32 [%0], [a], b, %3, e;\n\t}"
-      :: "r"(d_tmem), "r"(a_tmem), "l"(b0), "r"(idesc), "r"(accumulate)
-      : "memory");
-}
-
 // Order this thread's generic-proxy shared-memory writes before later
 // async-proxy (tensor core, TMA) reads of them.
 __device__ __forceinline__ void fence_proxy_async_smem() {
