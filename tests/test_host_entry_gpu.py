@@ -18,8 +18,8 @@ pytestmark = pytest.mark.gpu
 
 # (H, Hkv, D, T, start_pos, window, dtype).  The kv heads go to one group
 # when the call moves less than 4 MiB, two below 128 MiB, else four (at most
-# Hkv); each group has its own copies, kernel and (bf16, head_dim 128) the
-# workspace schedule pfa_prefill_attention_ws picks for its heads alone.
+# Hkv); each group has its own copies, kernel and (bf16) the workspace
+# schedule pfa_prefill_attention_ws picks for its heads alone.
 CASES = [
     (6, 2, 128, 150, 20, 0, "bf16"),       # 1 group, group size 3
     (4, 1, 128, 77, 9, 0, "bf16"),         # 1 group, one kv head
@@ -32,6 +32,7 @@ CASES = [
     (8, 8, 128, 64, 70000, 0, "bf16"),     # 287 MB: 4 groups, pairs past 64 key tiles
     (5, 5, 128, 32, 110000, 0, "bf16"),    # 282 MB: 4 uneven groups (1 + 1 + 1 + 2)
     (32, 8, 128, 128, 20000, 0, "bf16"),   # 84 MB: 2 groups, each on the balanced schedule
+    (32, 4, 512, 640, 4000, 0, "bf16"),    # 80 MB: 2 groups, each on the head_dim-512 tail split
 ]
 
 
@@ -66,7 +67,7 @@ def test_host_entry_matches_device_entry_and_oracle(case, pinned):
     assert G.digest(again) == G.digest(got)
     plain = all(pkg.schedule(T, sp, h, hkv, D, w, q.dtype)[0] == "plain"
                 for h, hkv in _groups(case))
-    if plain or dt != "bf16" or D != 128:
+    if plain or dt != "bf16":
         on_device = G.run(q, k, v, window=w, workspace=None)
         assert G.digest(got) == G.digest(on_device.cpu())
 
@@ -173,3 +174,10 @@ def test_host_entry_concurrent_callers():
         t.join()
     assert not errors, errors
     assert pkg.last_device_error() == 0
+
+
+def test_host_entry_groups_take_the_head_dim_512_tail_split():
+    """The case above exercises the tail split inside the host entry."""
+    H, Hkv, D, T, sp, w = 32, 4, 512, 640, 4000, 0
+    assert [pkg.schedule(T, sp, h, hkv, D, w)[0] for h, hkv in _groups((H, Hkv, D, T, sp, w, "bf16"))] \
+        == ["tail", "tail"]
