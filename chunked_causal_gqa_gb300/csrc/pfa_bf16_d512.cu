@@ -1,7 +1,8 @@
 // pfa_bf16_d512.cu -- fused flash-style prefill attention for bf16, head_dim 512
 // (the Gemma-style wide heads of the TensorSharp2 Gemma-4 prefill design,
 // section 2: the head_dim-512 flash kernel, and its sliding-window layers),
-// on the sm_103a tensor cores (tcgen05 + tensor memory + TMA).
+// on the sm_103a tensor cores (tcgen05 + tensor memory + TMA), with the two
+// CTAs of a cluster issuing their products together (cta_group::2).
 //
 // Operation: as for head_dim 128 (gnosis "Prefill attention -> GPU: handoff",
 // section "GPU design", steps 1-3, fused).
@@ -9,31 +10,46 @@
 // Budget that shapes this kernel: a 128 x 512 fp32 output accumulator would
 // fill all 512 columns of tensor memory, leaving none for the scores, and one
 // 128 x 512 bf16 query tile takes 128 KB of the 227 KB of shared memory.  So a
-// CTA owns one 128-row query tile (group heads x 128/group tokens) of one kv
-// head and one half (256 columns) of the output head dimension.  The two CTAs
-// of a tile both compute the full S = Q K^T (contraction over all 512
-// dimensions) and each accumulates its half of P V: 1.5x the minimum tensor
-// work, in exchange for fitting S and O in tensor memory.
+// CTA keeps one 128-row query tile (group heads x 128/group tokens) of one kv
+// head and one half (256 columns) of the output head dimension, and another
+// cluster computes the other half (both compute the full S = Q K^T: 1.5x the
+// minimum tensor work, in exchange for fitting S and O in tensor memory).
 //
-// Key tiles of 128: every QK^T product is M=128 N=128 K=16, so the query tile
-// (read from shared memory by every product) is read once per 128 keys.  K
-// (128 keys x 512) does not fit beside Q, so it streams through a ring of
-// 16 KB slots as eight 64-column chunks; this CTA's half of V streams as two
-// 64-key chunks of 32 KB (two slots each).  The producer fills the ring in
-// the order the MMA warp consumes it: K(0), K(1), V(0), K(2), V(1), ...
+// A 128-key tile needs the whole K tile (128 keys x 512) and the V rows of
+// this output half: 192 KB, more than one SM takes in from L2 while its
+// tensor core does the tile's 3k cycles of work.  So the two CTAs of a
+// cluster (ranks 0 and 1, on two SMs) take query tiles 2p and 2p + 1 of the
+// same kv head and output half, and rank 0 issues products of M = 256 rows
+// for both (tcgen05.mma.cta_group::2): each CTA supplies its own 128 query
+// rows (A) and half of the B operand -- keys 64 r .. 64 r + 63 of each K
+// tile, output columns 128 r .. 128 r + 127 of this half of each V tile --
+// and each CTA's tensor memory receives its own rows of S and O.  Every SM
+// then takes in 96 KB per key tile.  The pair walks the union of its two
+// tiles' key ranges; each CTA masks the keys its own rows do not see.
 //
-// Warp roles (6 warps):
+// Key tiles of 128: S products are M=256 N=128 K=16; the K slices stream
+// through a ring of six 16 KB slots (two 64-key x 64-column boxes per slot,
+// four slots per tile), this CTA's V slice as two slots (64 keys x 128
+// columns each).  The producer of each CTA fills its ring in the order rank
+// 0 consumes it: K(0), K(1), V(0), K(2), V(1), ...
+//
+// Warp roles (6 warps per CTA):
 //   warps 0-3  softmax and epilogue (TMEM lanes 0-127, one row per thread)
-//   warp  4    TMA producer: Q once, then the K and V chunks
-//   warp  5    TMEM allocator and MMA issuer (the whole warp runs the loop;
-//              one elected lane issues each group of tcgen05.mma)
+//   warp  4    TMA producer: Q once, then this CTA's K and V slices.  The
+//              loads of both CTAs complete on rank 0's barriers (TMA
+//              .cta_group::2), so rank 0 sees when a slot is full in both.
+//   warp  5    TMEM allocation (both ranks); on rank 0 the MMA issuer (one
+//              elected lane issues each group of tcgen05.mma for the pair)
 //
-// Tensor memory: [0,128) S_0, [128,256) S_1 (double-buffered scores; after the
-// softmax the first 64 columns hold P as packed bf16 pairs), [256,512) O half.
+// Tensor memory (each CTA): [0,128) S_0, [128,256) S_1 (double-buffered
+// scores; after the softmax the first 64 columns hold P as packed bf16
+// pairs), [256,512) O half.
 //
 // MMA issue order: S(0), S(1), O += P(0) V(0), S(2), O += P(1) V(1), ...
 // The softmax of tile i overlaps S(i+1); it waits for O += P(i-1) V(i-1)
-// (barrier kBarO, one phase per tile) before it may rescale O.
+// (barrier kBarO, one phase per tile) before it may rescale O.  Rank 0's
+// commits arrive on the barrier at the same offset in both CTAs; rank 1's
+// softmax warps arrive on rank 0's P barriers.
 #include "pfa_internal.h"
 #include "pfa_ptx.cuh"
 
@@ -48,14 +64,171 @@
 namespace pfa {
 namespace {
 
-constexpr int kBM = 128;                  // query rows per tile
+// ---------------------------------------------------------------- pairs of CTAs
+// Every tcgen05 instruction of this kernel that takes a CTA group uses
+// cta_group::2: the allocation is made by one warp of each CTA of the pair,
+// the products are issued by rank 0 and read both CTAs' shared and tensor
+// memory, and a commit arrives on the mbarrier at the given offset in each
+// CTA of the mask.  Measured on GB300: an mbarrier arrival with release at
+// cluster scope costs the arriving thread ~1.2k cycles; the arrivals below
+// use the default (CTA-scope) release, like the tensor-core pipeline's own
+// signals, and the waits acquire at cluster scope.
+
+__device__ __forceinline__ uint32_t cluster_ctarank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+// All threads of both CTAs: orders earlier shared-memory work (barrier
+// initialisation, remote arrivals) before the peer's later accesses.
+__device__ __forceinline__ void cluster_sync() {
+  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;"
+               ::: "memory");
+}
+// Address of the same shared-memory location in CTA `rank` of the cluster.
+__device__ __forceinline__ uint32_t cluster_addr(uint32_t local, uint32_t rank) {
+  uint32_t r;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(local), "r"(rank));
+  return r;
+}
+// Arrival on an mbarrier given by its cluster address (this CTA's or the
+// peer's).
+__device__ __forceinline__ void mbar_arrive_cluster(uint32_t cluster_bar) {
+  asm volatile("mbarrier.arrive.shared::cluster.b64 _, [%0];" :: "r"(cluster_bar) : "memory");
+}
+__device__ __forceinline__ bool mbar_try_wait_cl(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile("{\n\t.reg .pred p;\n\t"
+               "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
+               "selp.u32 %0, 1, 0, p;\n\t}"
+               : "=r"(ok) : "r"(bar), "r"(parity) : "memory");
+  return ok != 0;
+}
+// mbar_wait for a barrier the peer CTA arrives on (acquire at cluster
+// scope), executed by every lane of a converged warp; bounded in time like
+// every other wait.
+__device__ __forceinline__ bool mbar_wait_cl_warp(uint32_t bar, uint32_t parity,
+                                                  volatile int* abort_flag, unsigned* err,
+                                                  uint64_t limit_ns) {
+  bool ok = mbar_try_wait_cl(bar, parity);
+  if (!ok) {
+    const uint64_t t0 = globaltimer_ns();
+    for (uint32_t spin = 1;; ++spin) {
+      if (mbar_try_wait_cl(bar, parity)) {
+        ok = true;
+        break;
+      }
+      if ((spin & 15u) == 0) {
+        if (*abort_flag) break;
+        if (globaltimer_ns() - t0 > limit_ns) {
+          *abort_flag = 1;
+          atomicOr(err, kErrTimeout);
+          break;
+        }
+      }
+    }
+  }
+  return __all_sync(0xffffffffu, ok);
+}
+
+// 3-D tiled bulk tensor load into this CTA's shared memory whose completion
+// is signalled, as transaction bytes, on an mbarrier of either CTA of the
+// pair (given by its cluster address).  c0 must keep the copy 16-byte aligned.
+__device__ __forceinline__ void tma_load_3d_pair(uint32_t dst, const CUtensorMap* map,
+                                                 uint32_t cluster_bar, int c0, int c1, int c2) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.cta_group::2.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%3, %4, %5}], [%2];"
+      :: "r"(dst), "l"(reinterpret_cast<uint64_t>(map)), "r"(cluster_bar), "r"(c0), "r"(c1), "r"(c2)
+      : "memory");
+}
+
+__device__ __forceinline__ void tmem_alloc_pair(uint32_t dst_smem, uint32_t ncols) {
+  asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;"
+               :: "r"(dst_smem), "r"(ncols) : "memory");
+}
+__device__ __forceinline__ void tmem_relinquish_pair() {
+  asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void tmem_dealloc_pair(uint32_t taddr, uint32_t ncols) {
+  asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;"
+               :: "r"(taddr), "r"(ncols) : "memory");
+}
+
+// Eight K=16 steps of D (+)= A * B for the pair, both operands K-major in
+// 128-byte-swizzled tiles: steps 0-3 in the spans at a0 / b0, steps 4-7 in
+// the spans kAHalf16 / kBHalf16 further (16-byte units).  From one converged
+// warp; one elected lane issues.
+template <uint32_t kAHalf16, uint32_t kBHalf16>
+__device__ __forceinline__ void mma8_ss_pair(uint32_t d_tmem, uint64_t a0, uint64_t b0,
+                                             uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred e, acc;\n\t.reg .b64 a, b;\n\t"
+      "elect.sync _|e, 0xffffffff;\n\t"
+      "setp.ne.b32 acc, %4, 0;\n\t"
+      "@e tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, acc;\n\t"
+      "add.s64 a, %1, 2;  add.s64 b, %2, 2;\n\t"
+      "@e tcgen05.mma.cta_group::2.kind::f16 [%0], a, b, %3, e;\n\t"
+      "add.s64 a, %1, 4;  add.s64 b, %2, 4;\n\t"
+      "@e tcgen05.mma.cta_group::2.kind::f16 [%0], a, b, %3, e;\n\t"
+      "add.s64 a, %1, 6;  add.s64 b, %2, 6;\n\t"
+      "@e tcgen05.mma.cta_group::2.kind::f16 [%0], a, b, %3, e;\n\t"
+      "add.s64 a, %1, %5;  add.s64 b, %2, %9;\n\t"
+      "@e tcgen05.mma.cta_group::2.kind::f16 [%0], a, b, %3, e;\n\t"
+      "add.s64 a, %1, %6;  add.s64 b, %2, %10;\n\t"
+      "@e tcgen05.mma.cta_group::2.kind::f16 [%0], a, b, %3, e;\n\t"
+      "add.s64 a, %1, %7;  add.s64 b, %2, %11;\n\t"
+      "@e tcgen05.mma.cta_group::2.kind::f16 [%0], a, b, %3, e;\n\t"
+      "add.s64 a, %1, %8;  add.s64 b, %2, %12;\n\t"
+      "@e tcgen05.mma.cta_group::2.kind::f16 [%0], a, b, %3, e;\n\t}"
+      :: "r"(d_tmem), "l"(a0), "l"(b0), "r"(idesc), "r"(accumulate),
+         "n"(kAHalf16), "n"(kAHalf16 + 2), "n"(kAHalf16 + 4), "n"(kAHalf16 + 6),
+         "n"(kBHalf16), "n"(kBHalf16 + 2), "n"(kBHalf16 + 4), "n"(kBHalf16 + 6)
+      : "memory");
+}
+
+// Four K=16 steps of D (+)= A * B for the pair, A in tensor memory (columns
+// a_tmem + 8 kk, packed bf16 pairs) and B in shared memory (descriptor b0 +
+// kk * kBStep16, 16-byte units).
+template <uint32_t kBStep16>
+__device__ __forceinline__ void mma4_ts_pair(uint32_t d_tmem, uint32_t a_tmem, uint64_t b0,
+                                             uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred e, acc;\n\t.reg .b64 b;\n\t.reg .b32 a;\n\t"
+      "elect.sync _|e, 0xffffffff;\n\t"
+      "setp.ne.b32 acc, %4, 0;\n\t"
+      "@e tcgen05.mma.cta_group::2.kind::f16 [%0], [%1], %2, %3, acc;\n\t"
+      "add.s32 a, %1, 8;  add.s64 b, %2, %5;\n\t"
+      "@e tcgen05.mma.cta_group::2.kind::f16 [%0], [a], b, %3, e;\n\t"
+      "add.s32 a, %1, 16; add.s64 b, %2, %6;\n\t"
+      "@e tcgen05.mma.cta_group::2.kind::f16 [%0], [a], b, %3, e;\n\t"
+      "add.s32 a, %1, 24; add.s64 b, %2, %7;\n\t"
+      "@e tcgen05.mma.cta_group::2.kind::f16 [%0], [a], b, %3, e;\n\t}"
+      :: "r"(d_tmem), "r"(a_tmem), "l"(b0), "r"(idesc), "r"(accumulate),
+         "n"(kBStep16), "n"(2 * kBStep16), "n"(3 * kBStep16)
+      : "memory");
+}
+
+// Commit of the issuing thread's earlier products, arriving on the mbarrier
+// at offset `bar` in both CTAs of the pair.  From one converged warp.
+__device__ __forceinline__ void tc_commit_pair(uint32_t bar) {
+  asm volatile(
+      "{\n\t.reg .pred e;\n\telect.sync _|e, 0xffffffff;\n\t"
+      "@e tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64"
+      " [%0], %1;\n\t}"
+      :: "r"(bar), "h"((uint16_t)3) : "memory");
+}
+
+// ---------------------------------------------------------------- layout
+constexpr int kBM = 128;                  // query rows per CTA (M = 256 per pair)
 constexpr int kBN = 128;                  // keys per tile
-constexpr int kVKeys = 64;                // keys per V chunk
-constexpr int kDHalf = 256;               // output columns per CTA
+constexpr int kKeysPerCta = 64;           // keys of each K tile in one CTA's slots
+constexpr int kDHalf = 256;               // output columns per cluster
+constexpr int kDQuarter = 128;            // V columns in one CTA's slots
 constexpr int kQChunk = 128 * 128;        // 128 rows x 64 bf16 (one 128-byte swizzle span)
-constexpr int kSlot = 16384;              // ring slot: a K chunk, or half a V chunk
+constexpr int kSlot = 16384;              // ring slot: two 64 x 64 boxes
+constexpr int kBox = 8192;                // 64 rows x 64 bf16
 constexpr int kRing = 6;                  // ring slots
-constexpr int kVSub = kVKeys * 128;       // 64 keys x 64 bf16 of V (8 KB)
 constexpr int kSmemQ = 0;                 // 8 chunks: 128 KB
 constexpr int kSmemRing = 8 * kQChunk;    // 6 slots: 96 KB
 constexpr int kSmemBars = kSmemRing + kRing * kSlot;  // 229376
@@ -63,30 +236,34 @@ constexpr int kSmemAlloc = kSmemBars + 256 + 1024;
 constexpr int kThreads = 192;
 constexpr float kRescaleThreshold = 8.0f;
 
-constexpr int kBarQ = 0;
+// Rank 0's kBarQ and kBarFull count the bytes of both CTAs' loads; rank 1's
+// are unused.  kBarS, kBarO, kBarDrain and kBarEmpty receive rank 0's
+// commits in both CTAs.
+constexpr int kBarQ = 0;                  // both CTAs' Q have landed
 constexpr int kBarS = 1;                  // 2
-constexpr int kBarP = 3;                  // 2
+constexpr int kBarP = 3;                  // 2; rank 0: 8 arrivals (4 softmax warps per CTA)
 constexpr int kBarO = 5;                  // one phase per tile's P V
 constexpr int kBarDrain = 6;
-constexpr int kBarFull = 7;               // kRing
-constexpr int kBarEmpty = kBarFull + kRing;  // kRing
+constexpr int kBarFull = 7;               // kRing: the slot has landed in both CTAs
+constexpr int kBarEmpty = kBarFull + kRing;  // kRing: the pair has consumed the slot
 constexpr int kNumBars = kBarEmpty + kRing;
 static_assert(kNumBars * 8 + 8 <= 256, "barrier area");
 constexpr int kOffTmemSlot = kNumBars * 8;
 constexpr int kOffAbort = kOffTmemSlot + 4;
 
 constexpr uint32_t kColS = 0, kColO = 256;
-constexpr uint32_t kIdescQK = idesc_bf16_f32(kBM, kBN, false);
-constexpr uint32_t kIdescPV = idesc_bf16_f32(kBM, kDHalf, true);
+constexpr uint32_t kIdescQK = idesc_bf16_f32(2 * kBM, kBN, false);
+constexpr uint32_t kIdescPV = idesc_bf16_f32(2 * kBM, kDHalf, true);
 
 // Tail split (with a caller workspace): the whole waves of units run whole;
 // each unit of the last, partial wave is cut into `parts` equal key ranges
-// run as separate CTA pairs, part by part; a piece writes its unnormalised
-// output half, exponent base and row sum to a workspace slot, and
+// run as separate clusters, part by part; a piece writes its unnormalised
+// output halves, exponent bases and row sums to a workspace slot, and
 // merge512_kernel combines the pieces of each unit in key order.
 constexpr int kPlainMode = 0, kTailMode = 2;
-constexpr size_t kOHalfFloats = (size_t)kBM * kDHalf;                 // one CTA's O, [col/4][row][4]
-constexpr size_t kSlotFloats512 = 2 * kOHalfFloats + 2 * 2 * kBM;    // O halves, base[2][128], sum[2][128]
+constexpr size_t kOHalfFloats = (size_t)kBM * kDHalf;  // one CTA's O, [col/4][row][4]
+// per piece: O for (rank, half) = 4 blocks, then base[4][128], sum[4][128]
+constexpr size_t kPieceFloats = 4 * kOHalfFloats + 2 * 4 * kBM;
 
 struct Params {
   __nv_bfloat16* out;
@@ -104,6 +281,26 @@ struct Params {
   int flags;
 };
 
+// Key tiles [first, first + n) of a unit: the union of the ranges of its two
+// query tiles 2 pair and 2 pair + 1 (the second may lie past T).
+struct UnitKeys {
+  int64_t first;
+  int n;
+};
+__host__ __device__ inline UnitKeys unit_keys(int64_t T, int64_t start_pos, int tok_per_tile,
+                                              int window, int pair) {
+  const int64_t t0a = (int64_t)(2 * pair) * tok_per_tile;
+  int64_t t_end = t0a + 2 * (int64_t)tok_per_tile;
+  if (t_end > T) t_end = T;
+  const int64_t pos_first = start_pos + t0a;
+  int64_t kmin = 0;
+  if (window > 0 && pos_first - window + 1 > 0) kmin = pos_first - window + 1;
+  UnitKeys u;
+  u.first = kmin / kBN;
+  u.n = (int)((start_pos + t_end - 1) / kBN - u.first + 1);
+  return u;
+}
+
 template <bool kFoldScale, bool kDyn>
 __global__ void __launch_bounds__(kThreads, 1)
 bf16_d512_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
@@ -119,9 +316,11 @@ bf16_d512_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const uint64_t lim = p.wait_limit_ns;
+  const int rank = (int)cluster_ctarank();  // = blockIdx.x & 1 (clusters of two)
 
   // Chunk length and position: kernel parameters, or (graph entry, kDyn) read
   // from device memory at run time, with the grid sized for the largest T.
+  // Both CTAs of a cluster take every decision below from the same values.
   int64_t T = p.T, start_pos = p.start_pos;
   int tiles_per_head = p.tiles_per_head;
   if (kDyn) {
@@ -132,14 +331,16 @@ bf16_d512_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
       return;
     }
     tiles_per_head = (int)((T + p.tok_per_tile - 1) / p.tok_per_tile);
-    if ((int)(blockIdx.x >> 1) >= tiles_per_head * p.Hkv) return;  // nothing set up yet
+    if ((int)(blockIdx.x >> 2) >= ((tiles_per_head + 1) / 2) * p.Hkv) return;  // nothing set up yet
   }
+  const int npairs = (tiles_per_head + 1) / 2;
 
-  // CTA pair b (CTAs 2b and 2b+1, one per output half dh) runs unit b whole,
+  // Cluster c = blockIdx.x / 2 computes output half dh = c % 2 of unit c / 2,
   // or, past the whole waves of a tail split, part r of unit p1 + e.
-  // Unit: (kv head, query tile); latest tokens first.
-  const int dh = blockIdx.x & 1;
-  const int pidx = blockIdx.x >> 1;
+  // Unit: (kv head, pair of query tiles); latest tokens first.
+  const int cl = (int)(blockIdx.x >> 1);
+  const int dh = cl & 1;
+  const int pidx = cl >> 1;
   int rest = pidx, part = 0, slot = -1;
   if (p.mode == kTailMode && pidx >= p.p1) {
     const int j = pidx - p.p1;
@@ -148,16 +349,15 @@ bf16_d512_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
     slot = j;
   }
   const int kh = rest % p.Hkv;
-  const int tile = tiles_per_head - 1 - rest / p.Hkv;
+  const int pair = npairs - 1 - rest / p.Hkv;
+  const int tile = 2 * pair + rank;
   const int64_t t0 = (int64_t)tile * p.tok_per_tile;
-  const int64_t t_end = min(t0 + p.tok_per_tile, T);
   const int64_t pos_first = start_pos + t0;
   const int64_t pos_last = start_pos + t0 + p.tok_per_tile - 1;
-  const int64_t kmin = p.window > 0 ? max((int64_t)0, pos_first - p.window + 1) : 0;
-  const int n_unit = (int)((start_pos + t_end - 1) / kBN - kmin / kBN + 1);
-  const int kb = slot < 0 ? 0 : (int)((int64_t)n_unit * part / p.parts);
-  const int ke = slot < 0 ? n_unit : (int)((int64_t)n_unit * (part + 1) / p.parts);
-  const int64_t kt_first = kmin / kBN + kb;  // first key tile of this CTA's range
+  const UnitKeys uk = unit_keys(T, start_pos, p.tok_per_tile, p.window, pair);
+  const int kb = slot < 0 ? 0 : (int)((int64_t)uk.n * part / p.parts);
+  const int ke = slot < 0 ? uk.n : (int)((int64_t)uk.n * (part + 1) / p.parts);
+  const int64_t kt_first = uk.first + kb;  // first key tile of this cluster's range
   const int n = ke - kb;
   auto key_row = [&](int64_t key) -> int {
     return (int)(p.ring_rows > 0 ? key % p.ring_rows : key);
@@ -165,24 +365,23 @@ bf16_d512_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < kNumBars; ++i)
-      mbar_init(bar(i), (i == kBarP || i == kBarP + 1) ? 4u : 1u);  // P: one arrival per softmax warp
+      mbar_init(bar(i), (i == kBarP || i == kBarP + 1) ? 8u : 1u);  // P: one arrival per softmax warp of the pair
     *abort_flag = 0;
     fence_mbar_init();
   }
   if (warp == 5) {
-    tmem_alloc(smem_u32(tmem_slot), 512);
-    tmem_relinquish();
+    tmem_alloc_pair(smem_u32(tmem_slot), 512);
+    tmem_relinquish_pair();
   }
   tc_fence_before();
   __syncthreads();
+  cluster_sync();  // the peer's barriers are initialised before any remote arrival
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
 
-  // Ring order (producer and consumer): for i = 0..n-1: the eight K chunks of
-  // tile i, then (i >= 1) the V chunks of tile i-1; after the last tile, the V
-  // chunks of tile n-1.  A V chunk is two consecutive slot loads; with eight
-  // K loads per tile its pair always starts on an even slot of the 6-slot
-  // ring, so its 32 KB are contiguous.
+  // Ring order (producers and consumer): for i = 0..n-1: the four K slots of
+  // tile i, then (i >= 1) the two V slots of tile i-1; after the last tile,
+  // the V slots of tile n-1.  Six loads per tile.
 
   if (warp == 4) {
     // ------------------------------------------------------------ producer
@@ -191,39 +390,45 @@ bf16_d512_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
       tma_prefetch_desc(&tm_k);
       tma_prefetch_desc(&tm_v);
       const int hq = kh * p.group;
-      mbar_arrive_expect_tx(bar(kBarQ), 8u * 128u * (uint32_t)(p.group * p.tok_per_tile));
+      // rank 0 arms its barrier for the bytes of both CTAs; rank 1's bytes
+      // may land first (the phase cannot complete before rank 0's arrival)
+      const uint32_t bar0 = cluster_addr(bar(0), 0);  // rank 0's barrier area
+      auto bar_r0 = [&](int i) -> uint32_t { return bar0 + 8u * (uint32_t)i; };
+      if (rank == 0)
+        mbar_arrive_expect_tx(bar(kBarQ), 2u * 8u * 128u * (uint32_t)(p.group * p.tok_per_tile));
       for (int c = 0; c < 8; ++c)
-        tma_load_3d(sbase + kSmemQ + c * kQChunk, &tm_q, bar(kBarQ), 64 * c, hq, (int)t0);
+        tma_load_3d_pair(sbase + kSmemQ + c * kQChunk, &tm_q, bar_r0(kBarQ), 64 * c, hq, (int)t0);
       uint32_t li = 0;  // slot loads issued
       bool ok = true;
       auto slot_wait = [&](uint32_t* dst) -> bool {
         const uint32_t s = li % kRing, ph = (li / kRing) & 1u;
         if (!mbar_wait(bar(kBarEmpty + s), ph ^ 1u, abort_flag, p.err, lim)) return false;
-        mbar_arrive_expect_tx(bar(kBarFull + s), (uint32_t)kSlot);
+        if (rank == 0) mbar_arrive_expect_tx(bar(kBarFull + s), 2u * (uint32_t)kSlot);
         *dst = s;
         return true;
       };
-      auto load_k = [&](int i) -> bool {
-        const int row = key_row((kt_first + i) * kBN);
-        for (int c = 0; c < 8; ++c) {
+      auto load_k = [&](int i) -> bool {  // keys 64 rank .. +63 of tile i, all 512 columns
+        const int row = key_row((kt_first + i) * kBN + kKeysPerCta * rank);
+        for (int c = 0; c < 4; ++c) {
           uint32_t s;
           if (!slot_wait(&s)) return false;
-          tma_load_3d(sbase + kSmemRing + s * kSlot, &tm_k, bar(kBarFull + s), 64 * c, row, kh);
+          for (int b = 0; b < 2; ++b)
+            tma_load_3d_pair(sbase + kSmemRing + s * kSlot + b * kBox, &tm_k, bar_r0(kBarFull + s),
+                             128 * c + 64 * b, row, kh);
           ++li;
         }
         return true;
       };
-      auto load_v = [&](int i) -> bool {
+      auto load_v = [&](int i) -> bool {  // columns 128 rank .. +127 of this half
+        const int col = dh * kDHalf + kDQuarter * rank;
         for (int h = 0; h < 2; ++h) {
-          const int row = key_row((kt_first + i) * kBN + h * kVKeys);
-          for (int part = 0; part < 2; ++part) {
-            uint32_t s;
-            if (!slot_wait(&s)) return false;
-            for (int b = 0; b < 2; ++b)
-              tma_load_3d(sbase + kSmemRing + s * kSlot + b * kVSub, &tm_v, bar(kBarFull + s),
-                          dh * kDHalf + 64 * (2 * part + b), row, kh);
-            ++li;
-          }
+          const int row = key_row((kt_first + i) * kBN + kKeysPerCta * h);
+          uint32_t s;
+          if (!slot_wait(&s)) return false;
+          for (int b = 0; b < 2; ++b)
+            tma_load_3d_pair(sbase + kSmemRing + s * kSlot + b * kBox, &tm_v, bar_r0(kBarFull + s),
+                             col + 64 * b, row, kh);
+          ++li;
         }
         return true;
       };
@@ -232,15 +437,19 @@ bf16_d512_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
         if (ok && i > 0) ok = load_v(i - 1);
       }
       if (ok) ok = load_v(n - 1);
-      // No copy may be in flight when the CTA exits.  On the normal path the
-      // MMA warp has already consumed every load, so these return at once.
-      mbar_wait(bar(kBarQ), 0, abort_flag, p.err, lim, true);
-      const uint32_t first = li > (uint32_t)kRing ? li - kRing : 0;
-      for (uint32_t j = first; j < li; ++j)
-        mbar_wait(bar(kBarFull + j % kRing), (j / kRing) & 1u, abort_flag, p.err, lim, true);
+      // No copy may be in flight when either CTA exits: rank 0 waits for the
+      // last loads of both (its barriers count both CTAs' bytes) before the
+      // final cluster barrier.  On the normal path the pair has already
+      // consumed every load, so these return at once.
+      if (rank == 0) {
+        mbar_wait(bar(kBarQ), 0, abort_flag, p.err, lim, true);
+        const uint32_t first = li > (uint32_t)kRing ? li - kRing : 0;
+        for (uint32_t j = first; j < li; ++j)
+          mbar_wait(bar(kBarFull + j % kRing), (j / kRing) & 1u, abort_flag, p.err, lim, true);
+      }
     }
-  } else if (warp == 5) {
-    // ------------------------------------------------------------ MMA issuer
+  } else if (warp == 5 && rank == 0) {
+    // ------------------------------------------------------------ MMA issuer (rank 0)
     // The whole warp runs this loop (operands stay warp-uniform); one elected
     // lane issues each group of MMAs and each commit.
     {
@@ -257,49 +466,50 @@ bf16_d512_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
         return true;
       };
       auto pv = [&](int j) -> bool {  // O (+)= P(j) V(j)
-        if (!mbar_wait_warp(bar(kBarP + (j & 1)), (uint32_t)(j >> 1) & 1u, abort_flag, p.err, lim))
+        if (!mbar_wait_cl_warp(bar(kBarP + (j & 1)), (uint32_t)(j >> 1) & 1u, abort_flag, p.err,
+                               lim))
           return false;
+        tc_fence_after();
         const uint32_t tP = tmem + kColS + (uint32_t)((j & 1) * kBN);
         for (int h = 0; h < 2; ++h) {
-          uint32_t s0, s1;
-          if (!slot_ready(&s0)) return false;
+          uint32_t s;
+          if (!slot_ready(&s)) return false;
           ++li;
-          if (!slot_ready(&s1)) return false;
-          ++li;
-          // 64 keys = 4 steps of 16 (2048 B apart); N = 256 spans the 4
-          // 64-column chunks of this CTA's V half (LBO = one chunk, 8 KB)
-          mma4_ts<2048 / 16>(tO, tP + 32u * h, sdesc_sw128(sbase + kSmemRing + s0 * kSlot, kVSub, 1024),
-                             kIdescPV, (j > 0 || h > 0) ? 1u : 0u);
-          tc_commit_elect(bar(kBarEmpty + s0));
-          tc_commit_elect(bar(kBarEmpty + s1));
+          // 64 keys = 4 steps of 16 (2048 B apart); each CTA's 128 columns are
+          // two 64-column boxes (LBO = one box, 8 KB)
+          mma4_ts_pair<2048 / 16>(tO, tP + 32u * h, sdesc_sw128(sbase + kSmemRing + s * kSlot, kBox, 1024),
+                                  kIdescPV, (j > 0 || h > 0) ? 1u : 0u);
+          tc_commit_pair(bar(kBarEmpty + s));
         }
-        tc_commit_elect(bar(kBarO));
+        tc_commit_pair(bar(kBarO));
         return true;
       };
       for (int i = 0; i < n && ok; ++i) {
         const uint32_t tS = tmem + kColS + (uint32_t)((i & 1) * kBN);
 #pragma unroll 1
-        for (int c = 0; c < 8 && ok; ++c) {
+        for (int c = 0; c < 4 && ok; ++c) {
           uint32_t s;
           if (!(ok = slot_ready(&s))) break;
-          mma4_ss_kmajor(tS, sdesc_sw128(sbase + kSmemQ + c * kQChunk, 16, 1024),
-                         sdesc_sw128(sbase + kSmemRing + s * kSlot, 16, 1024), kIdescQK,
-                         c > 0 ? 1u : 0u);
+          // Q columns 128 c .. 128 c + 127 (chunks 2c, 2c + 1) against the two
+          // 64-column boxes of the slot
+          mma8_ss_pair<kQChunk / 16, kBox / 16>(
+              tS, sdesc_sw128(sbase + kSmemQ + 2 * c * kQChunk, 16, 1024),
+              sdesc_sw128(sbase + kSmemRing + s * kSlot, 16, 1024), kIdescQK, c > 0 ? 1u : 0u);
           issued = true;
-          tc_commit_elect(bar(kBarEmpty + s));
+          tc_commit_pair(bar(kBarEmpty + s));
           ++li;
         }
         if (!ok) break;
-        tc_commit_elect(bar(kBarS + (i & 1)));
+        tc_commit_pair(bar(kBarS + (i & 1)));
         if (i > 0 && !(ok = pv(i - 1))) break;
       }
       if (ok) ok = pv(n - 1);
       if (issued) {
-        tc_commit_elect(bar(kBarDrain));
+        tc_commit_pair(bar(kBarDrain));
         mbar_wait_warp(bar(kBarDrain), 0, abort_flag, p.err, lim, true);
       }
     }
-  } else {
+  } else if (warp < 4) {
     // ------------------------------------------------------------ softmax
     const int row = warp * 32 + lane;
     const int tok = row / p.group;
@@ -311,6 +521,7 @@ bf16_d512_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
     const uint32_t lane_off = (uint32_t)(warp * 32) << 16;
     const uint32_t tO = tmem + lane_off + kColO;
     const float c = p.scale_log2;
+    const uint32_t bar_p[2] = {cluster_addr(bar(kBarP), 0), cluster_addr(bar(kBarP + 1), 0)};  // rank 0's
 
     float m_run = -INFINITY, l = 0.f;
     bool ok = true;
@@ -419,7 +630,7 @@ bf16_d512_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
       tmem_wait_st();
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(bar(kBarP + (i & 1)));
+      if (lane == 0) mbar_arrive_cluster(bar_p[i & 1]);
     }
     if (ok) {
       ok = mbar_wait(bar(kBarO), (uint32_t)(n - 1) & 1u, abort_flag, p.err, lim);
@@ -428,8 +639,9 @@ bf16_d512_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
     if (ok && slot >= 0) {
       // piece of a split unit: unnormalised fp32 output half, base and sum
       tc_fence_after();
-      float* ws = p.ws + (size_t)slot * kSlotFloats512;
-      float4* ocol = reinterpret_cast<float4*>(ws + (size_t)dh * kOHalfFloats) + row;
+      const int blk = rank * 2 + dh;
+      float* ws = p.ws + (size_t)slot * kPieceFloats;
+      float4* ocol = reinterpret_cast<float4*>(ws + (size_t)blk * kOHalfFloats) + row;
 #pragma unroll 1
       for (int c0 = 0; c0 < kDHalf; c0 += 32) {
         uint32_t o[32];
@@ -441,8 +653,8 @@ bf16_d512_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
               make_float4(__uint_as_float(o[4 * j]), __uint_as_float(o[4 * j + 1]),
                           __uint_as_float(o[4 * j + 2]), __uint_as_float(o[4 * j + 3]));
       }
-      ws[2 * kOHalfFloats + dh * 2 * kBM + row] = m_run;
-      ws[2 * kOHalfFloats + dh * 2 * kBM + kBM + row] = l;
+      ws[4 * kOHalfFloats + blk * kBM + row] = m_run;
+      ws[4 * kOHalfFloats + 4 * kBM + blk * kBM + row] = l;
     } else if (ok) {
       tc_fence_after();
       const float inv = l > 0.f ? 1.f / l : 0.f;
@@ -466,25 +678,31 @@ bf16_d512_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
     }
   }
 
+  // Neither CTA leaves, nor frees tensor memory, while the pair's products
+  // or copies may still touch it: rank 0 drains both before this point.
   tc_fence_before();
   __syncthreads();
+  cluster_sync();
   if (warp == 5) {
     tc_fence_after();
-    tmem_dealloc(tmem, 512);
+    tmem_dealloc_pair(tmem, 512);
   }
 }
 
 // Combines the pieces of each split unit in key order:
 // m = max_r m_r, O = sum_r 2^(m_r - m) O_r, l = sum_r 2^(m_r - m) l_r, out = O / l.
-// Block (e, g): unit p1 + e, output columns 16 g .. 16 g + 15; thread = row
-// (the pieces' [col/4][row][4] layout makes every load coalesced).
+// Block (e, g, rank): query tile 2 pair + rank of unit p1 + e, output columns
+// 16 g .. 16 g + 15; thread = row (the pieces' [col/4][row][4] layout makes
+// every load coalesced).
 constexpr int kMerge512Cols = 16;
 
 __global__ void __launch_bounds__(kBM) merge512_kernel(const Params p) {
   const int e = blockIdx.x;
   const int unit = p.p1 + e;
+  const int rank = blockIdx.z;
   const int kh = unit % p.Hkv;
-  const int tile = p.tiles_per_head - 1 - unit / p.Hkv;
+  const int npairs = (p.tiles_per_head + 1) / 2;
+  const int tile = 2 * (npairs - 1 - unit / p.Hkv) + rank;
   const int row = threadIdx.x;
   const int tok = row / p.group;
   const int64_t t = (int64_t)tile * p.tok_per_tile + tok;
@@ -492,23 +710,24 @@ __global__ void __launch_bounds__(kBM) merge512_kernel(const Params p) {
   const int h = kh * p.group + row % p.group;
   const int col0 = blockIdx.y * kMerge512Cols;
   const int dh = col0 / kDHalf;
+  const int blk = rank * 2 + dh;
   const int cq0 = (col0 % kDHalf) / 4;  // first column quad within the half
-  auto slot = [&](int r) -> const float* {
-    return p.ws + (size_t)(r * p.p2 + e) * kSlotFloats512;
+  auto piece = [&](int r) -> const float* {
+    return p.ws + (size_t)(r * p.p2 + e) * kPieceFloats;
   };
-  const size_t off_m = 2 * kOHalfFloats + (size_t)dh * 2 * kBM + row, off_l = off_m + kBM;
+  const size_t off_m = 4 * kOHalfFloats + (size_t)blk * kBM + row, off_l = off_m + 4 * kBM;
   float m = -INFINITY;
-  for (int r = 0; r < p.parts; ++r) m = fmaxf(m, slot(r)[off_m]);
+  for (int r = 0; r < p.parts; ++r) m = fmaxf(m, piece(r)[off_m]);
   const float mb = (m == -INFINITY) ? 0.f : m;
   float4 acc[kMerge512Cols / 4];
 #pragma unroll
   for (int q = 0; q < kMerge512Cols / 4; ++q) acc[q] = make_float4(0.f, 0.f, 0.f, 0.f);
   float l = 0.f;
   for (int r = 0; r < p.parts; ++r) {
-    const float* ws = slot(r);
+    const float* ws = piece(r);
     const float w = ex2(ws[off_m] - mb);  // 0 for a piece that saw no visible key
     l = fmaf(w, ws[off_l], l);
-    const float4* ocol = reinterpret_cast<const float4*>(ws + (size_t)dh * kOHalfFloats) + row;
+    const float4* ocol = reinterpret_cast<const float4*>(ws + (size_t)blk * kOHalfFloats) + row;
 #pragma unroll
     for (int q = 0; q < kMerge512Cols / 4; ++q) {
       const float4 o = ocol[(size_t)(cq0 + q) * kBM];
@@ -538,25 +757,15 @@ struct Plan512 {
   size_t ws_bytes = 0;
 };
 
-// Key tiles of unit u, as the kernel derives them.
-int unit_tiles(const Call& c, int tiles_per_head, int tok_per_tile, int u) {
-  const int tile = tiles_per_head - 1 - u / c.Hkv;
-  const int64_t t0 = (int64_t)tile * tok_per_tile;
-  const int64_t t_end = std::min<int64_t>(t0 + tok_per_tile, c.T);
-  const int64_t pos_first = c.start_pos + t0;
-  const int64_t kmin = c.window > 0 ? std::max<int64_t>(0, pos_first - c.window + 1) : 0;
-  return (int)((c.start_pos + t_end - 1) / kBN - kmin / kBN + 1);
-}
-
-// Fixed cost of a CTA (Q load, pipeline fill, epilogue) and of the merge, in
-// key-tile units.
+// Fixed cost of a cluster (Q load, pipeline fill, epilogue) and of the
+// merge, in key-tile units.
 constexpr int64_t kCtaOverheadTiles = 2, kMerge512CostTiles = 2;
 constexpr int kMaxParts512 = 8;
 
-// Makespan, in key-tile units, of CTAs launched in order on `sms` SMs (the
-// hardware starts each on the first SM that frees up).
-int64_t makespan(const std::vector<int64_t>& costs, int sms) {
-  std::vector<int64_t> free_at((size_t)std::max(sms, 1), 0);
+// Makespan, in key-tile units, of clusters launched in order on `slots`
+// pairs of SMs (the hardware starts each on the first pair that frees up).
+int64_t makespan(const std::vector<int64_t>& costs, int slots) {
+  std::vector<int64_t> free_at((size_t)std::max(slots, 1), 0);
   int64_t end = 0;
   for (int64_t cost : costs) {
     std::pop_heap(free_at.begin(), free_at.end(), std::greater<int64_t>());
@@ -568,27 +777,32 @@ int64_t makespan(const std::vector<int64_t>& costs, int sms) {
 }
 
 // The tail split is taken when it beats the plain schedule's estimate by 5%.
+// Units (kv head, pair of query tiles) take four CTAs: two clusters, one per
+// output half.
 Plan512 plan_d512(const Call& c) {
   Plan512 plan;
-  if (c.lens != nullptr || c.num_sms < 2) return plan;
+  if (c.lens != nullptr || c.num_sms < 4) return plan;
   const int group = c.H / c.Hkv;
   const int tok_per_tile = kBM / group;
   const int64_t tiles = (c.T + tok_per_tile - 1) / tok_per_tile;
-  const int64_t U = tiles * c.Hkv;
-  const int per_wave = c.num_sms / 2;  // units (CTA pairs) per wave
+  const int64_t npairs = (tiles + 1) / 2;
+  const int64_t U = npairs * c.Hkv;
+  const int per_wave = c.num_sms / 4;  // units per wave
+  const int slots = c.num_sms / 2;     // clusters in flight
   if (U <= per_wave || U > (1 << 20)) return plan;
   const int p1 = per_wave * (int)(U / per_wave), p2 = (int)(U - p1);
   if (p2 == 0) return plan;
   std::vector<int> n((size_t)U);
   int nmin = INT32_MAX;
   for (int u = 0; u < (int)U; ++u) {
-    n[u] = unit_tiles(c, (int)tiles, tok_per_tile, u);
+    const int pair = (int)npairs - 1 - u / c.Hkv;
+    n[u] = unit_keys(c.T, c.start_pos, tok_per_tile, c.window, pair).n;
     if (u >= p1) nmin = std::min(nmin, n[u]);
   }
   std::vector<int64_t> costs;
   for (int u = 0; u < (int)U; ++u)
     for (int d = 0; d < 2; ++d) costs.push_back(n[u] + kCtaOverheadTiles);
-  const int64_t plain = makespan(costs, c.num_sms);
+  const int64_t plain = makespan(costs, slots);
   int64_t best = INT64_MAX;
   for (int parts = 2; parts <= kMaxParts512 && parts <= nmin; ++parts) {
     costs.clear();
@@ -600,7 +814,7 @@ Plan512 plan_d512(const Call& c) {
         for (int d = 0; d < 2; ++d)
           costs.push_back(nu * (r + 1) / parts - nu * r / parts + kCtaOverheadTiles);
       }
-    const int64_t m = makespan(costs, c.num_sms) + kMerge512CostTiles;
+    const int64_t m = makespan(costs, slots) + kMerge512CostTiles;
     if (m < best) {
       best = m;
       plan.parts = parts;
@@ -610,7 +824,7 @@ Plan512 plan_d512(const Call& c) {
   plan.mode = kTailMode;
   plan.p1 = p1;
   plan.p2 = p2;
-  plan.ws_bytes = (size_t)p2 * plan.parts * kSlotFloats512 * sizeof(float);
+  plan.ws_bytes = (size_t)p2 * plan.parts * kPieceFloats * sizeof(float);
   return plan;
 }
 
@@ -639,8 +853,9 @@ int launch_bf16_d512(const Call& c) {
   const int group = c.H / c.Hkv;
   const int tok_per_tile = kBM / group;
   const int64_t tiles = (c.T + tok_per_tile - 1) / tok_per_tile;
+  const int64_t npairs = (tiles + 1) / 2;
   const int64_t L = c.start_pos + c.T;
-  if (2 * tiles * c.Hkv > 0x7fffffff || L + kBN > 0x7fffffff) return kErrShape;
+  if (4 * npairs * c.Hkv > 0x7fffffff || L + 2 * kBN > 0x7fffffff) return kErrShape;
 
   CUtensorMap tq, tk, tv;
   {
@@ -650,13 +865,13 @@ int launch_bf16_d512(const Call& c) {
     if (encode_tmap_bf16_3d(&tq, c.q, dims, strides, box)) return kErrLaunch;
   }
   {
-    // Rows past the written part of the cache read as zeros.
+    // Rows past the written part of the cache read as zeros.  K and V move
+    // in boxes of 64 keys x 64 columns.
     const uint64_t dims[3] = {512, (uint64_t)cache_rows_written(c), (uint64_t)c.Hkv};
     const uint64_t strides[2] = {512 * 2, (uint64_t)c.max_seq_len * 512 * 2};
-    const uint32_t kbox[3] = {64, (uint32_t)kBN, 1};     // a K chunk: 128 keys x 64 columns
-    const uint32_t vbox[3] = {64, (uint32_t)kVKeys, 1};  // a V box: 64 keys x 64 columns
-    if (encode_tmap_bf16_3d(&tk, c.k, dims, strides, kbox)) return kErrLaunch;
-    if (encode_tmap_bf16_3d(&tv, c.v, dims, strides, vbox)) return kErrLaunch;
+    const uint32_t box[3] = {64, (uint32_t)kKeysPerCta, 1};
+    if (encode_tmap_bf16_3d(&tk, c.k, dims, strides, box)) return kErrLaunch;
+    if (encode_tmap_bf16_3d(&tv, c.v, dims, strides, box)) return kErrLaunch;
   }
   // the tail split when the caller gave a large enough workspace
   Plan512 plan;
@@ -687,24 +902,34 @@ int launch_bf16_d512(const Call& c) {
   p.err = c.err;
   p.wait_limit_ns = c.wait_limit_ns;
   p.flags = c.flags;
-  const int64_t pairs = plan.mode == kTailMode
+  const int64_t units = plan.mode == kTailMode
                             ? (int64_t)plan.p1 + (int64_t)plan.p2 * plan.parts
-                            : tiles * c.Hkv;
-  const dim3 grid((unsigned)(2 * pairs));
+                            : npairs * c.Hkv;
+  // Clusters of two consecutive CTAs: the two query tiles of a unit, for one
+  // output half.
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)(4 * units));
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = kSmemAlloc;
+  cfg.stream = c.stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
   const bool fold = p.scale_log2 > 0.f;
-  if (c.lens) {
-    if (fold)
-      bf16_d512_kernel<true, true><<<grid, kThreads, kSmemAlloc, c.stream>>>(tq, tk, tv, p);
-    else
-      bf16_d512_kernel<false, true><<<grid, kThreads, kSmemAlloc, c.stream>>>(tq, tk, tv, p);
-  } else if (fold) {
-    bf16_d512_kernel<true, false><<<grid, kThreads, kSmemAlloc, c.stream>>>(tq, tk, tv, p);
-  } else {
-    bf16_d512_kernel<false, false><<<grid, kThreads, kSmemAlloc, c.stream>>>(tq, tk, tv, p);
-  }
-  if (cudaGetLastError() != cudaSuccess) return kErrLaunch;
+  cudaError_t e;
+  if (c.lens)
+    e = fold ? cudaLaunchKernelEx(&cfg, bf16_d512_kernel<true, true>, tq, tk, tv, p)
+             : cudaLaunchKernelEx(&cfg, bf16_d512_kernel<false, true>, tq, tk, tv, p);
+  else
+    e = fold ? cudaLaunchKernelEx(&cfg, bf16_d512_kernel<true, false>, tq, tk, tv, p)
+             : cudaLaunchKernelEx(&cfg, bf16_d512_kernel<false, false>, tq, tk, tv, p);
+  if (e != cudaSuccess || cudaGetLastError() != cudaSuccess) return kErrLaunch;
   if (plan.mode == kTailMode) {
-    merge512_kernel<<<dim3((unsigned)plan.p2, 512 / kMerge512Cols), kBM, 0, c.stream>>>(p);
+    merge512_kernel<<<dim3((unsigned)plan.p2, 512 / kMerge512Cols, 2), kBM, 0, c.stream>>>(p);
     if (cudaGetLastError() != cudaSuccess) return kErrLaunch;
   }
   return kOk;
