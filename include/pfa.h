@@ -227,8 +227,8 @@ PFA_API int pfa_workspace_bytes(int64_t T, int64_t start_pos, int num_heads, int
  * which pfa_last_device_error returns.  T == 0 writes nothing.
  *
  * Cache rows past L: the host cannot clip the tensor maps at a run-time L, so
- * for PFA_BF16 the rows of the last 128-key tile (64 for head_dim 512) past
- * L are read and weighted by exactly zero -- they must hold finite values
+ * for PFA_BF16 the rows of the last 128-key tile past L are read and
+ * weighted by exactly zero -- they must hold finite values
  * (never-written rows of a zero-initialised cache do).  The fp32 path reads
  * no row past L.
  *
@@ -249,8 +249,9 @@ PFA_API int pfa_prefill_attention_graph(const void *q, const void *k_cache, cons
  * on the current device when its workspace is at least *workspace_bytes
  * (the value pfa_workspace_bytes reports):
  *   PFA_SCHEDULE_PLAIN     one kernel, one CTA per pair of 128-row query tiles
- *                          (head_dim 512: two CTAs per query tile, one per
- *                          half of the output columns);
+ *                          (head_dim 512: per pair of query tiles, two
+ *                          clusters of two CTAs, one cluster per half of the
+ *                          output columns);
  *   PFA_SCHEDULE_BALANCED  equal-cost runs of key-tile ranges per SM, then a
  *                          merge kernel (two launches);
  *   PFA_SCHEDULE_TAIL      the whole waves of pairs run whole and the pairs
@@ -258,9 +259,8 @@ PFA_API int pfa_prefill_attention_graph(const void *q, const void *k_cache, cons
  *                          ranges (with no more pairs than SMs: every pair
  *                          is cut, the CTAs of one range running together),
  *                          then a merge kernel (two launches).  head_dim 512
- *                          has this schedule (with query tiles in place of
- *                          pairs, and without the every-pair form) and the
- *                          plain one; fp32 has the plain one only.
+ *                          has this schedule (without the every-pair form)
+ *                          and the plain one; fp32 has the plain one only.
  * Same validation as pfa_workspace_bytes; nothing is launched.  Returns
  * PFA_OK and sets both outputs, or an error status.
  */
