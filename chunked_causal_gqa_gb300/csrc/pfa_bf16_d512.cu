@@ -219,6 +219,14 @@ __device__ __forceinline__ void tc_commit_pair(uint32_t bar) {
       :: "r"(bar), "h"((uint16_t)3) : "memory");
 }
 
+// 32 bytes (eight 32-bit words) to a 32-byte aligned global address.
+__device__ __forceinline__ void st_global_v8(void* dst, const uint32_t* w) {
+  asm volatile("st.global.v8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};"
+               :: "l"(dst), "r"(w[0]), "r"(w[1]), "r"(w[2]), "r"(w[3]), "r"(w[4]), "r"(w[5]),
+                  "r"(w[6]), "r"(w[7])
+               : "memory");
+}
+
 // ---------------------------------------------------------------- layout
 constexpr int kBM = 128;                  // query rows per CTA (M = 256 per pair)
 constexpr int kBN = 128;                  // keys per tile
@@ -270,6 +278,7 @@ struct Params {
   float* ws;         // tail split: the pieces' slots; else null
   int mode, p1, p2, parts;
   int64_t o_stride;  // elements from one token's output row to the next
+  int out_v8;        // output rows start on 32-byte boundaries
   int ring_rows;     // > 0: key j is in cache row j % ring_rows; 0: in row j
   int64_t T, start_pos;          // graph entry: T = the largest T, start_pos unused
   const int64_t* lens;           // graph entry: device {T, start_pos}; else null
@@ -657,22 +666,34 @@ bf16_d512_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
       ws[4 * kOHalfFloats + 4 * kBM + blk * kBM + row] = l;
     } else if (ok) {
       tc_fence_after();
+      // Each thread writes its row's 512 contiguous bytes: with 32-byte
+      // aligned rows, in 32-byte stores (whole L2 sectors; measured 57.7 ->
+      // 55.6 us on the window layer against 16-byte stores).
       const float inv = l > 0.f ? 1.f / l : 0.f;
       __nv_bfloat16* orow = p.out + (t * p.o_stride + h * (int64_t)512 + dh * kDHalf);
 #pragma unroll 1
-      for (int c0 = 0; c0 < kDHalf; c0 += 32) {
-        uint32_t o[32];
+      for (int c0 = 0; c0 < kDHalf; c0 += 64) {
+        uint32_t o[32], o2[32];
         tmem_ld32(tO + c0, o);
+        tmem_ld32(tO + c0 + 32, o2);
         tmem_wait_ld(o);
-        uint32_t w[16];
+        tmem_wait_ld(o2);
+        uint32_t w[32];
 #pragma unroll
-        for (int j = 0; j < 16; ++j)
+        for (int j = 0; j < 16; ++j) {
           w[j] = pack_bf16x2(__uint_as_float(o[2 * j]) * inv, __uint_as_float(o[2 * j + 1]) * inv);
+          w[16 + j] = pack_bf16x2(__uint_as_float(o2[2 * j]) * inv, __uint_as_float(o2[2 * j + 1]) * inv);
+        }
         if (row_valid) {
-          uint4* dst = reinterpret_cast<uint4*>(orow + c0);
+          if (p.out_v8) {
 #pragma unroll
-          for (int j = 0; j < 4; ++j)
-            dst[j] = make_uint4(w[4 * j], w[4 * j + 1], w[4 * j + 2], w[4 * j + 3]);
+            for (int j = 0; j < 4; ++j) st_global_v8(orow + c0 + 16 * j, &w[8 * j]);
+          } else {
+            uint4* dst = reinterpret_cast<uint4*>(orow + c0);
+#pragma unroll
+            for (int j = 0; j < 8; ++j)
+              dst[j] = make_uint4(w[4 * j], w[4 * j + 1], w[4 * j + 2], w[4 * j + 3]);
+          }
         }
       }
     }
@@ -887,6 +908,7 @@ int launch_bf16_d512(const Call& c) {
   p.p2 = plan.p2;
   p.parts = plan.parts;
   p.o_stride = c.qkv_dim;
+  p.out_v8 = (reinterpret_cast<uintptr_t>(c.out) % 32 == 0 && c.qkv_dim % 16 == 0) ? 1 : 0;
   p.ring_rows = ring_rows(c);
   p.T = c.T;
   p.start_pos = c.start_pos;

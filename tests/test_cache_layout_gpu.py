@@ -68,6 +68,7 @@ LINEAR = [
     (257, 0, 8, 2, 128, 0, "bf16", 8, 1000, False),
     (200, 500, 8, 2, 128, 129, "bf16", 128, 77, False),
     (130, 100, 8, 2, 512, 0, "bf16", 512, 200, False),
+    (130, 100, 8, 2, 512, 0, "bf16", 8, 200, False),      # rows 16 B (not 32 B) aligned
     (77, 30, 8, 2, 64, 0, "f32", 4, 50, False),
     (40, 10, 4, 1, 128, 7, "f32", 128, 1, False),
 ]
