@@ -320,16 +320,20 @@ def run_ours(args, wl):
         pkg.prefill_attention(q, k, v, out=out, window=wl.window, scale=wl.scale,
                               workspace=workspace)
 
+    # The clock sampler starts before the warm-up, so that no idle gap (its
+    # start-up) separates the warm-up from the timed steps: after ~0.3 s of
+    # idle the first timed steps of a short workload ran slower.
+    sampler = ClockSampler(int(os.environ.get("CUDA_VISIBLE_DEVICES", str(local)).split(",")[0])
+                           if os.environ.get("CUDA_VISIBLE_DEVICES", "").isdigit() else local)
+    sampler.start()
     for _ in range(args.warmup):
         flush.fill_(1)
         step()
     torch.cuda.synchronize(dev)
     if pkg.last_device_error() != 0:
+        sampler.stop()
         raise RuntimeError("device error during warm-up")
 
-    sampler = ClockSampler(int(os.environ.get("CUDA_VISIBLE_DEVICES", str(local)).split(",")[0])
-                           if os.environ.get("CUDA_VISIBLE_DEVICES", "").isdigit() else local)
-    sampler.start()
     # one sustained burst so that the clock sampler sees the GPU under load
     events = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
               for _ in range(args.steps)]
