@@ -28,7 +28,7 @@ EXPORTS = ("pfa_prefill_attention", "pfa_prefill_attention_ws", "pfa_workspace_b
            "pfa_prefill_attention_host", "pfa_host_buffer_bytes",
            "pfa_status_string",
            "pfa_last_device_error", "pfa_version", "pfa_debug_configure",
-           "pfa_debug_check_schedule")
+           "pfa_debug_check_schedule", "pfa_debug_check_schedule_d512")
 
 _lock = threading.Lock()
 _lib = None
@@ -96,6 +96,8 @@ def load(path: str | None = None) -> ctypes.CDLL:
         ip = ctypes.POINTER(i32)
         lib.pfa_debug_check_schedule.argtypes = [i64, i64, i32, i32, i32, i32, ip, ip, ip]
         lib.pfa_debug_check_schedule.restype = i32
+        lib.pfa_debug_check_schedule_d512.argtypes = [i64, i64, i32, i32, i32, i32, ip, ip, ip]
+        lib.pfa_debug_check_schedule_d512.restype = i32
         if path is None:
             _lib = lib
         return lib

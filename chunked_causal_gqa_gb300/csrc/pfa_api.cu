@@ -579,6 +579,34 @@ int pfa_debug_check_schedule(int64_t T, int64_t start_pos, int num_heads, int nu
   return PFA_OK;
 }
 
+int pfa_debug_check_schedule_d512(int64_t T, int64_t start_pos, int num_heads, int num_kv_heads,
+                                  int window, int num_sms, int* schedule, int* ctas,
+                                  int* failed_check) {
+  if (!schedule || !ctas || !failed_check) return PFA_ERR_NULL;
+  *schedule = 0;
+  *ctas = 0;
+  *failed_check = 0;
+  if (num_sms <= 0 || num_sms > 1024) return PFA_ERR_SHAPE;
+  // shape checks of the bf16 head_dim-512 path, without a device
+  if (T < 0 || start_pos < 0 || num_heads <= 0 || num_kv_heads <= 0 ||
+      num_heads % num_kv_heads != 0 || num_heads / num_kv_heads > 128)
+    return PFA_ERR_SHAPE;
+  const int64_t L = start_pos + T;
+  if (L > ((int64_t)1 << 31) - 4096) return PFA_ERR_SHAPE;
+  if (T == 0) return PFA_OK;
+  Call c{};
+  c.T = T;
+  c.start_pos = start_pos;
+  c.H = num_heads;
+  c.Hkv = num_kv_heads;
+  c.D = 512;
+  c.window = window > 0 ? window : 0;
+  c.qkv_dim = (int64_t)num_heads * 512;
+  c.max_seq_len = L;
+  *failed_check = check_schedule_bf16_d512(c, num_sms, schedule, ctas);
+  return PFA_OK;
+}
+
 int pfa_host_buffer_bytes(int64_t T, int64_t start_pos, int num_heads, int num_kv_heads,
                           int head_dim, int window, int dtype, size_t* bytes) {
   if (!bytes) return PFA_ERR_NULL;

@@ -851,6 +851,109 @@ Plan512 plan_d512(const Call& c) {
 
 }  // namespace
 
+// Host replay of the work assignment of a launch (schedule of `c` on `sms`
+// SMs): the kernel's CTA -> (cluster, rank, item) mapping, run for every CTA
+// of the grid, and the merge's reads.  Returns 0, or the number of the first
+// failed check.
+int check_schedule_bf16_d512(const Call& c0, int sms, int* schedule, int* ctas) {
+  Call c = c0;
+  c.num_sms = sms;
+  c.lens = nullptr;
+  const Plan512 plan = plan_d512(c);
+  *schedule = plan.mode == kTailMode ? 2 : 0;
+  const int group = c.H / c.Hkv;
+  const int tok_per_tile = kBM / group;
+  const int64_t tiles = (c.T + tok_per_tile - 1) / tok_per_tile;
+  const int npairs = (int)((tiles + 1) / 2);
+  const int64_t units = plan.mode == kTailMode ? (int64_t)plan.p1 + (int64_t)plan.p2 * plan.parts
+                                               : (int64_t)npairs * c.Hkv;
+  const int64_t grid = 4 * units;
+  if (grid > (1 << 24)) return 1;
+  *ctas = (int)grid;
+  const int64_t L = c.start_pos + c.T;
+  const int pieces = plan.mode == kTailMode ? plan.p2 * plan.parts : 0;
+  struct Cover {
+    int64_t kb, ke;
+    int slot;
+  };
+  std::vector<std::vector<Cover>> cover((size_t)(c.Hkv * tiles * 2));
+  std::vector<int> slot_ctas((size_t)pieces, 0);
+  for (int64_t b = 0; b < grid; ++b) {
+    const int rank = (int)(b & 1), cl = (int)(b >> 1), dh = cl & 1, pidx = cl >> 1;
+    int rest = pidx, part = 0, slot = -1;
+    if (plan.mode == kTailMode && pidx >= plan.p1) {
+      const int j = pidx - plan.p1;
+      part = j / plan.p2;
+      rest = plan.p1 + j % plan.p2;
+      slot = j;
+    }
+    const int kh = rest % c.Hkv;
+    const int pair = npairs - 1 - rest / c.Hkv;
+    if (kh < 0 || kh >= c.Hkv || pair < 0 || pair >= npairs) return 2;
+    const UnitKeys uk = unit_keys(c.T, c.start_pos, tok_per_tile, c.window, pair);
+    const int kb = slot < 0 ? 0 : (int)((int64_t)uk.n * part / plan.parts);
+    const int ke = slot < 0 ? uk.n : (int)((int64_t)uk.n * (part + 1) / plan.parts);
+    if (uk.n < 1 || ke <= kb) return 3;                       // every cluster walks a key tile
+    if (uk.first < 0 || (uk.first + uk.n - 1) * kBN > L - 1) return 4;  // tiles start inside the cache
+    // TMA x coordinates of the 64-column boxes: Q and K at 64 q, V at this
+    // CTA's columns of the half: 16-byte aligned and inside the 512 columns
+    for (int q = 0; q < 8; ++q)
+      if ((64 * q) % 8 || 64 * q + 64 > 512) return 5;
+    for (int bb = 0; bb < 2; ++bb) {
+      const int x = dh * kDHalf + kDQuarter * rank + 64 * bb;
+      if (x % 8 || x + 64 > 512) return 5;
+    }
+    const int tile = 2 * pair + rank;
+    const int64_t t0 = (int64_t)tile * tok_per_tile;
+    if (t0 >= c.T) {
+      if (tile != tiles || rank != 1) return 6;  // only the second tile of an odd last pair
+      continue;
+    }
+    for (int64_t t = t0; t < t0 + tok_per_tile && t < c.T; ++t) {
+      const int64_t pos = c.start_pos + t;
+      const int64_t lo = c.window > 0 ? std::max<int64_t>(0, pos - c.window + 1) : 0;
+      if (lo < uk.first * kBN || pos >= (uk.first + uk.n) * kBN) return 7;  // visible keys walked
+    }
+    if (slot >= 0) {
+      if (slot >= pieces) return 8;
+      ++slot_ctas[(size_t)slot];
+    }
+    cover[(size_t)((kh * tiles + tile) * 2 + dh)].push_back({uk.first + kb, uk.first + ke, slot});
+  }
+  for (int j = 0; j < pieces; ++j)
+    if (slot_ctas[(size_t)j] != 4) return 9;  // a piece slot: both ranks, both halves
+  for (int kh = 0; kh < c.Hkv; ++kh)
+    for (int64_t tile = 0; tile < tiles; ++tile) {
+      const int pair = (int)(tile / 2);
+      const UnitKeys uk = unit_keys(c.T, c.start_pos, tok_per_tile, c.window, pair);
+      const int unit = (npairs - 1 - pair) * c.Hkv + kh;
+      const bool split = plan.mode == kTailMode && unit >= plan.p1;
+      for (int dh = 0; dh < 2; ++dh) {
+        std::vector<Cover> v = cover[(size_t)((kh * tiles + tile) * 2 + dh)];
+        std::sort(v.begin(), v.end(), [](const Cover& a, const Cover& b) { return a.kb < b.kb; });
+        if (!split) {
+          // one whole item writes the output
+          if (v.size() != 1 || v[0].slot >= 0 || v[0].kb != uk.first || v[0].ke != uk.first + uk.n)
+            return 10;
+          continue;
+        }
+        // the pieces cover the unit's key tiles in order, and the merge of
+        // unit p1 + e reads exactly their slots r * p2 + e, r = 0 .. parts-1
+        if ((int)v.size() != plan.parts) return 11;
+        const int e = unit - plan.p1;
+        int64_t at = uk.first;
+        for (int r = 0; r < plan.parts; ++r) {
+          if (v[(size_t)r].kb != at || v[(size_t)r].slot != r * plan.p2 + e) return 12;
+          at = v[(size_t)r].ke;
+        }
+        if (at != uk.first + uk.n) return 13;
+      }
+    }
+  if (plan.mode == kTailMode && plan.ws_bytes < (size_t)pieces * kPieceFloats * sizeof(float))
+    return 14;
+  return 0;
+}
+
 size_t workspace_bytes_bf16_d512(const Call& c, int* schedule) {
   const Plan512 plan = plan_d512(c);
   if (schedule) *schedule = plan.mode == kTailMode ? 2 : 0;

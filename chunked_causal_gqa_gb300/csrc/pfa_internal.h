@@ -124,5 +124,7 @@ inline size_t workspace_bytes_bf16(const Call& c, int* schedule = nullptr) {
 // Host-only replay of the head_dim-128 work assignment with its invariants
 // (pfa_debug_check_schedule); 0 or the number of the failed check.
 int check_schedule_bf16_d128(const Call& c, int sms, int* schedule, int* ctas);
+// The same for the head_dim-512 path (pfa_debug_check_schedule_d512).
+int check_schedule_bf16_d512(const Call& c, int sms, int* schedule, int* ctas);
 
 }  // namespace pfa

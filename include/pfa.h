@@ -418,6 +418,24 @@ PFA_API int pfa_debug_check_schedule(int64_t T, int64_t start_pos, int num_heads
                                      int num_kv_heads, int window, int num_sms, int *schedule,
                                      int *ctas, int *failed_check);
 
+/*
+ * pfa_debug_check_schedule_d512 -- test hook, host only (no device is
+ * touched): the same replay for the bf16 head_dim-512 path -- every CTA of the
+ * grid mapped to its cluster, rank (query tile of the pair), output half and
+ * key-tile range, and the merge's reads -- with its invariants: every output
+ * half of every query tile is written by exactly one whole item or merged from
+ * pieces that cover its pair's key tiles in order from distinct workspace
+ * slots (each filled by the pair's two CTAs for both halves) that fit the
+ * workspace; every cluster walks at least one key tile, its key tiles start
+ * inside the cache and cover every key visible to its rows; the TMA boxes'
+ * column coordinates are 16-byte aligned and inside the head; a query tile
+ * past T occurs only as the second tile of an odd last pair.
+ * Outputs and return values as for pfa_debug_check_schedule.
+ */
+PFA_API int pfa_debug_check_schedule_d512(int64_t T, int64_t start_pos, int num_heads,
+                                          int num_kv_heads, int window, int num_sms,
+                                          int *schedule, int *ctas, int *failed_check);
+
 /* Library ABI version: (major << 16) | minor. */
 PFA_API int pfa_version(void);
 

@@ -45,6 +45,9 @@ int main(void)
         CHECK(10, pfa_debug_check_schedule(2048, 61440, 32, 8, 0, 152, &schedule, &ctas,
                                            &failed) == PFA_OK);
         CHECK(11, schedule == PFA_SCHEDULE_TAIL && failed == 0);
+        CHECK(16, pfa_debug_check_schedule_d512(2048, 6144, 8, 2, 1024, 152, &schedule, &ctas,
+                                                &failed) == PFA_OK);
+        CHECK(17, schedule == PFA_SCHEDULE_PLAIN && ctas == 256 && failed == 0);
     }
     {
         /* the host-buffer entry: checks that need no device */

@@ -66,3 +66,50 @@ def test_arguments_are_checked(lib):
                                         ctypes.byref(kind), ctypes.byref(kind)) == -2
     assert lib.pfa_debug_check_schedule(16, 0, 8, 2, 0, 0, ctypes.byref(kind),
                                         ctypes.byref(kind), ctypes.byref(kind)) == -2
+
+
+# ---- head_dim 512: pairs of CTAs (clusters) per pair of query tiles and output half
+
+def check512(lib, T, sp, H, Hkv, window, sms):
+    kind, ctas, failed = ctypes.c_int(-1), ctypes.c_int(-1), ctypes.c_int(-1)
+    rc = lib.pfa_debug_check_schedule_d512(T, sp, H, Hkv, window, sms, ctypes.byref(kind),
+                                           ctypes.byref(ctas), ctypes.byref(failed))
+    assert rc == 0, (T, sp, H, Hkv, window, sms, rc)
+    return kind.value, ctas.value, failed.value
+
+
+SHAPES512 = list(itertools.product(
+    [1, 33, 40, 130, 640, 650, 2048],           # T (odd and even tile counts)
+    [0, 5, 129, 4000, 6144, 20000],             # start_pos
+    [(8, 2), (16, 2), (4, 4), (6, 2), (8, 1), (32, 4)],  # (H, Hkv): groups 4, 8, 1, 3, 8, 8
+    [0, 1, 64, 1024],                           # window
+))
+
+
+@pytest.mark.parametrize("sms", [152, 148, 132, 17])
+def test_every_head_dim_512_schedule_keeps_its_invariants(lib, sms):
+    kinds = set()
+    for T, sp, (H, Hkv), w in SHAPES512:
+        kind, ctas, failed = check512(lib, T, sp, H, Hkv, w, sms)
+        assert failed == 0, f"check {failed} failed for T={T} sp={sp} H={H}/{Hkv} w={w} sms={sms}"
+        assert ctas > 0 and ctas % 4 == 0
+        kinds.add(kind)
+    assert kinds == {0, 2}, kinds   # plain and tail split both exercised
+
+
+def test_head_dim_512_workloads_get_the_expected_schedules(lib):
+    # Gemma-style layers (2048 tokens of 8/2 heads at 6144): plain, 2 x 2 x 32 x 2 CTAs
+    assert check512(lib, 2048, 6144, 8, 2, 0, 152) == (0, 256, 0)
+    assert check512(lib, 2048, 6144, 8, 2, 1024, 152) == (0, 256, 0)
+    # 640 tokens of 16/2 heads at 4000: 40 units on 38 per wave -> tail split
+    kind, ctas, failed = check512(lib, 640, 4000, 16, 2, 0, 152)
+    assert kind == 2 and failed == 0 and ctas > 4 * 40
+    # odd number of query tiles (7 per head): the last pair's second tile is past T
+    assert check512(lib, 200, 100, 8, 2, 0, 152) == (0, 32, 0)
+
+
+def test_head_dim_512_check_arguments(lib):
+    kind = ctypes.c_int()
+    assert lib.pfa_debug_check_schedule_d512(16, 0, 8, 2, 0, 152, None, None, None) == -1
+    assert lib.pfa_debug_check_schedule_d512(16, 0, 6, 4, 0, 152, ctypes.byref(kind),
+                                             ctypes.byref(kind), ctypes.byref(kind)) == -2
