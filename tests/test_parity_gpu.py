@@ -36,13 +36,17 @@ BF16_CASES = [
     (8, 2, 128, 200, 0, 1000),     # window longer than the prompt
     (8, 2, 128, 1, 0, 0),          # a single first token
     (8, 2, 128, 1, 777, 0),        # a single token deep in the cache
-    # head_dim 512 (key tiles of 128, each CTA owning half of the output columns)
-    (8, 2, 512, 200, 100, 0),
+    # head_dim 512 (key tiles of 128; a cluster of two CTAs per pair of query
+    # tiles and half of the output columns)
+    (8, 2, 512, 200, 100, 0),      # 7 tiles per head: the last pair's second tile past T
     (8, 2, 512, 130, 0, 64),       # window of exactly one key tile
     (8, 2, 512, 150, 300, 1000),   # window longer than the visible prefix
-    (4, 4, 512, 150, 10, 0),       # group 1
+    (4, 4, 512, 150, 10, 0),       # group 1: 128 tokens per tile
     (8, 1, 512, 40, 300, 100),     # group 8
-    (6, 2, 512, 70, 5, 0),         # group 3
+    (6, 2, 512, 70, 5, 0),         # group 3: 126-row tiles
+    (16, 1, 512, 50, 300, 0),      # group 16: 8 tokens per tile, 7 tiles
+    (32, 1, 512, 33, 1000, 200),   # group 32: 4 tokens per tile, window
+    (128, 1, 512, 5, 7, 0),        # group 128: 1 token per tile, odd count
     (8, 2, 512, 1, 50, 0),
 ]
 
