@@ -391,9 +391,10 @@ def test_tail_split_on_a_windowed_layer():
             "plain+window")
 
 
-# head_dim 512 with a last, partial wave of query tiles: the tail split cuts
-# each tile of that wave into equal key ranges (groups of 8 heads: 16 tokens
-# per tile; 80 or 82 tiles on 76 CTA pairs per wave).
+# head_dim 512 with a last, partial wave of units: the tail split cuts each
+# unit of that wave into equal key ranges (groups of 8 heads: 16 tokens per
+# tile; 40 or 42 units -- pairs of query tiles of one kv head, four CTAs each
+# -- on 38 per wave).
 D512_TAIL_CASES = [
     (16, 2, 512, 640, 4000, 0),
     (16, 2, 512, 650, 4000, 0),      # ragged T
