@@ -63,12 +63,21 @@ def kernel_name(wl) -> str:
     return f"bf16_d{wl.head_dim}"
 
 
+# Headers a kernel's source includes besides pfa_ptx.cuh (part of its hash).
+KERNEL_HEADERS = {
+    "bf16_d512": ("chunked_causal_gqa_gb300/csrc/pfa_pair.cuh",),
+    "f32x3_d128": ("chunked_causal_gqa_gb300/csrc/pfa_pair.cuh",),
+}
+
+
 def source_hash(name: str) -> str:
     path = os.path.join(ROOT, KERNEL_SOURCES.get(name, ""))
     if not os.path.isfile(path):
         return ""
     h = hashlib.sha256()
-    for p in (path, os.path.join(ROOT, "chunked_causal_gqa_gb300/csrc/pfa_ptx.cuh")):
+    files = (path, os.path.join(ROOT, "chunked_causal_gqa_gb300/csrc/pfa_ptx.cuh")) + \
+        tuple(os.path.join(ROOT, f) for f in KERNEL_HEADERS.get(name, ()))
+    for p in files:
         with open(p, "rb") as f:
             h.update(f.read())
     return h.hexdigest()[:16]

@@ -18,26 +18,36 @@
 // three-product tf32 form it replaces needed the tf32 rate, half the bf16
 // rate, on operands twice as large.
 //
-// CTA = one kv head x one 128-row query tile (all `group` query heads of the
-// kv head for 128/group consecutive tokens; row r -> token r/group, head
-// r%group); CTAs in kv-head-major order, latest tokens first within a head.
-// Key tiles of 128.
+// Pairs of CTAs.  The two CTAs of a cluster (ranks 0 and 1, on two SMs) take
+// query tiles 2p and 2p + 1 of one kv head (each: all `group` query heads for
+// 128/group consecutive tokens; row r -> token r/group, head r%group), and
+// rank 0 issues products of M = 256 rows for both (tcgen05.mma.cta_group::2):
+// each CTA supplies its own query rows and half of the B operand -- keys
+// 64 r .. 64 r + 63 of each K tile, columns 64 r .. 64 r + 63 of each V tile
+// -- so each SM converts half of every fp32 K and V tile.  (With one CTA per
+// tile, each SM converted whole tiles, and the conversion, not the tensor
+// core, set the pace.)  The pair walks the union of its two tiles' key
+// ranges; each CTA masks the keys its own rows do not see.  Clusters in
+// kv-head-major order, latest tokens first within a head.  Key tiles of 128.
 //
-// Warp roles (9 warps):
+// Warp roles (9 warps per CTA):
 //   warps 0-3  rows of the tile (TMEM lanes 0-127, one row per thread): split
 //              Q into hi/lo operand tiles in shared memory once, then the
 //              online softmax of every key tile, then the epilogue
-//   warps 4-7  converters: read fp32 K and V tiles from global memory (ring
-//              and strided caches included), split them into hi/lo bf16 and
-//              write the 128-byte-swizzled operand layout a TMA load of a bf16
-//              tile would produce, into a 5-slot ring (one slot = one 128x128
-//              bf16 tile; a K or V tile takes two slots, hi and lo)
-//   warp  8    TMEM allocator and MMA issuer (converged warp, elected lane)
+//   warps 4-7  converters: read this CTA's half of the fp32 K and V tiles
+//              from global memory (ring and strided caches included), split
+//              them into hi/lo bf16 and write the 128-byte-swizzled operand
+//              layout a TMA load of a bf16 tile would produce, into a ring of
+//              5 items (an item: hi and lo of one K or V half, 32 KB)
+//   warp  8    TMEM allocation (both ranks); on rank 0 the MMA issuer
+//              (converged warp, elected lane)
+// Rank 0's barriers for operands, Q and P count the arrivals of both CTAs'
+// warps; rank 0's commits arrive on the barrier at the same offset in both.
 //
-// Tensor memory (512 columns): [0,128) S_0 and [128,256) S_1 (double-buffered
-// scores; after the softmax P_hi, packed bf16 pairs, fills the first 64
-// columns of its buffer), [256,384) O, [384,448) and [448,512) P_lo of the two
-// buffers.
+// Tensor memory (each CTA, 512 columns): [0,128) S_0 and [128,256) S_1
+// (double-buffered scores; after the softmax P_hi, packed bf16 pairs, fills
+// the first 64 columns of its buffer), [256,384) O, [384,448) and [448,512)
+// P_lo of the two buffers.
 //
 // MMA issue order: S(0), S(1), O += P(0) V(0), S(2), O += P(1) V(1), ...
 // so that while the softmax of tile i runs, the tensor core executes
@@ -48,6 +58,7 @@
 // kernels (the exponent base rises only when a row maximum exceeds it by more
 // than 2^8); masks come from indices; every wait is bounded.
 #include "pfa_internal.h"
+#include "pfa_pair.cuh"
 #include "pfa_ptx.cuh"
 
 #include <cmath>
@@ -60,21 +71,25 @@ constexpr int kBM = 128;                   // query rows per CTA
 constexpr int kBN = 128;                   // keys per tile
 constexpr int kThreads = 288;
 constexpr int kHalfBytes = 128 * 128;      // 128 rows x 64 bf16 (one 128-byte swizzle span)
-constexpr int kTileBytes = 2 * kHalfBytes; // 128 rows x 128 bf16
-constexpr int kSlots = 5;                  // operand ring depth (bf16 tiles)
+constexpr int kTileBytes = 2 * kHalfBytes; // 128 rows x 128 bf16 (the Q operand tiles)
+constexpr int kPartBytes = 16384;          // one CTA's half of a K or V operand tile (hi or lo)
+constexpr int kKSpan = 8192;               // K half: 64 keys x 64 columns per 128-byte span
+constexpr int kItems = 5;                  // operand ring depth (items: hi + lo of a K or V half)
+constexpr int kItemBytes = 2 * kPartBytes;
 constexpr int kSmemQHi = 0;
 constexpr int kSmemQLo = kTileBytes;
 constexpr int kSmemRing = 2 * kTileBytes;
-constexpr int kSmemBars = kSmemRing + kSlots * kTileBytes;  // 229376
+constexpr int kSmemBars = kSmemRing + kItems * kItemBytes;  // 229376
 constexpr int kSmemAlloc = kSmemBars + 256 + 1024;
 constexpr float kRescaleThreshold = 8.0f;  // log2 units
 
-// barriers
-constexpr int kBarQ = 0;                        // Q hi/lo written (4 row-warp arrivals)
-constexpr int kBarFull = 1;                     // kSlots: operand tile written (4 converter arrivals)
-constexpr int kBarEmpty = kBarFull + kSlots;    // kSlots: operand tile consumed (commit)
-constexpr int kBarS = kBarEmpty + kSlots;       // 2: S(i) complete (commit)
-constexpr int kBarP = kBarS + 2;                // 2: P(i) in TMEM (4 row-warp arrivals)
+// barriers (rank 0's count both CTAs' arrivals; rank 1's kBarQ, kBarFull and
+// kBarP are unused)
+constexpr int kBarQ = 0;                        // Q hi/lo written (8 row-warp arrivals)
+constexpr int kBarFull = 1;                     // kItems: operand item written (8 converter arrivals)
+constexpr int kBarEmpty = kBarFull + kItems;    // kItems: operand item consumed (commit)
+constexpr int kBarS = kBarEmpty + kItems;       // 2: S(i) complete (commit)
+constexpr int kBarP = kBarS + 2;                // 2: P(i) in TMEM (8 row-warp arrivals)
 constexpr int kBarO = kBarP + 2;                // O += P(i) V(i) complete (commit), one phase per tile
 constexpr int kBarDrain = kBarO + 1;
 constexpr int kNumBars = kBarDrain + 1;
@@ -83,8 +98,8 @@ constexpr int kOffAbort = kOffTmemSlot + 4;
 static_assert(kOffAbort + 4 <= 256, "barrier area");
 
 constexpr uint32_t kColO = 256, kColPLo = 384;
-constexpr uint32_t kIdescQK = idesc_bf16_f32(kBM, kBN, false);  // K-major Q and K
-constexpr uint32_t kIdescPV = idesc_bf16_f32(kBM, kD, true);    // V is N(=d)-contiguous
+constexpr uint32_t kIdescQK = idesc_bf16_f32(2 * kBM, kBN, false);  // K-major Q and K
+constexpr uint32_t kIdescPV = idesc_bf16_f32(2 * kBM, kD, true);    // V is N(=d)-contiguous
 
 struct Params {
   const float* q;
@@ -134,11 +149,13 @@ __device__ __forceinline__ void prefetch_l2(const void* ptr, uint32_t bytes) {
 }
 
 // Byte offset of the 8-byte piece holding elements 4q .. 4q+3 (q = 0..31) of
-// row r in a 128-byte-swizzled K-major bf16 tile of 128 rows x 128 elements:
-// 64-element spans 16 KB apart, row r at r * 128, 16-byte chunk c at c ^ (r % 8).
+// row r in a 128-byte-swizzled K-major bf16 tile of `rows` rows x 128
+// elements: 64-element spans rows * 128 bytes apart, row r at r * 128, 16-byte
+// chunk c at c ^ (r % 8).
+template <int kRows>
 __device__ __forceinline__ uint32_t swz_off(int r, int q) {
   const int span = q >> 4, c = (q & 15) >> 1, half = q & 1;
-  return (uint32_t)(span * kHalfBytes + r * 128 + ((c ^ (r & 7)) << 4) + half * 8);
+  return (uint32_t)(span * (kRows * 128) + r * 128 + ((c ^ (r & 7)) << 4) + half * 8);
 }
 
 __global__ void __launch_bounds__(kThreads, 1) f32x3_d128_kernel(const Params p) {
@@ -152,9 +169,11 @@ __global__ void __launch_bounds__(kThreads, 1) f32x3_d128_kernel(const Params p)
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + kSmemBars + kOffAbort);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const uint64_t lim = p.wait_limit_ns;
+  const int rank = (int)cluster_ctarank();  // = blockIdx.x & 1 (clusters of two)
 
   // Chunk length and position: kernel parameters, or (graph entry) read from
-  // device memory at run time, with the grid sized for the largest T.
+  // device memory at run time, with the grid sized for the largest T.  Both
+  // CTAs of a cluster take every decision below from the same values.
   int64_t T = p.T, start_pos = p.start_pos;
   int tiles_per_head = p.tiles_per_head;
   if (p.lens) {
@@ -165,115 +184,121 @@ __global__ void __launch_bounds__(kThreads, 1) f32x3_d128_kernel(const Params p)
       return;
     }
     tiles_per_head = (int)((T + p.tok_per_tile - 1) / p.tok_per_tile);
-    if ((int)blockIdx.x >= tiles_per_head * p.Hkv) return;  // nothing set up yet
   }
+  const int pairs_per_head = (tiles_per_head + 1) / 2;
+  const int cl = (int)(blockIdx.x >> 1);
+  if (p.lens && cl >= pairs_per_head * p.Hkv) return;  // nothing set up yet
 
-  // work unit: (kv head, query tile), kv head major, latest tokens first
-  // within a head: the CTAs in flight cover few kv heads, so the fp32 K/V
-  // they stream (16 MB per head at 16k keys) stays in L2 between them
-  const int kh = (int)blockIdx.x / tiles_per_head;
-  const int tile = tiles_per_head - 1 - (int)blockIdx.x % tiles_per_head;
-  const int64_t t0 = (int64_t)tile * p.tok_per_tile;
-  const int64_t t_end = min(t0 + p.tok_per_tile, T);
-  const int64_t pos_first = start_pos + t0;
-  const int64_t pos_last = start_pos + t_end - 1;
-  const int64_t kmin = p.window > 0 ? max((int64_t)0, pos_first - p.window + 1) : 0;
+  // Unit of cluster cl: (kv head, pair of query tiles), kv head major, latest
+  // tokens first within a head: the clusters in flight cover few kv heads, so
+  // the fp32 K/V they stream (16 MB per head at 16k keys) stays in L2
+  // between them.  This CTA's tile is 2 pair + rank (past T for the second
+  // tile of an odd last pair: its rows hold no token).
+  const int kh = cl / pairs_per_head;
+  const int pair = pairs_per_head - 1 - cl % pairs_per_head;
+  const int64_t t0 = (int64_t)(2 * pair + rank) * p.tok_per_tile;
+  const int64_t t0a = (int64_t)(2 * pair) * p.tok_per_tile;
+  const int64_t t_end = min(t0a + 2 * (int64_t)p.tok_per_tile, T);  // end of the pair's tokens
+  const int64_t kmin = p.window > 0 ? max((int64_t)0, start_pos + t0a - p.window + 1) : 0;
   const int64_t kt_first = kmin / kBN;
-  const int n = (int)(pos_last / kBN - kt_first + 1);
+  const int n = (int)((start_pos + t_end - 1) / kBN - kt_first + 1);
   const int64_t L = start_pos + T;
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < kNumBars; ++i) {
       const bool per_warp = (i == kBarQ || i == kBarP || i == kBarP + 1 ||
-                             (i >= kBarFull && i < kBarFull + kSlots));
-      mbar_init(bar(i), per_warp ? 4u : 1u);
+                             (i >= kBarFull && i < kBarFull + kItems));
+      mbar_init(bar(i), per_warp ? 8u : 1u);
     }
     *abort_flag = 0;
     fence_mbar_init();
   }
   if (warp == 8) {
-    tmem_alloc(smem_u32(tmem_slot), 512);
-    tmem_relinquish();
+    tmem_alloc_pair(smem_u32(tmem_slot), 512);
+    tmem_relinquish_pair();
   }
   tc_fence_before();
   __syncthreads();
+  cluster_sync();  // the peer's barriers are initialised before any remote arrival
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
+  const uint32_t bar0 = cluster_addr(bars, 0);  // rank 0's barrier area
+  auto bar_r0 = [&](int i) -> uint32_t { return bar0 + 8u * (uint32_t)i; };
 
   // Ring order (converters and MMA warp), items u = 0 .. 2n-1: K(0); then for
-  // i = 1 .. n-1: K(i), V(i-1); then V(n-1).  Each item is two consecutive
-  // slot loads: hi, lo.
+  // i = 1 .. n-1: K(i), V(i-1); then V(n-1).  Item u occupies ring entry
+  // u % kItems: hi at its start, lo 16 KB further.
 
-  if (warp == 8) {
-    // ------------------------------------------------------------ MMA issuer
-    bool ok = mbar_wait_warp(bar(kBarQ), 0, abort_flag, p.err, lim);
+  if (warp == 8 && rank == 0) {
+    // ------------------------------------------------------------ MMA issuer (rank 0)
+    bool ok = mbar_wait_cl_warp(bar(kBarQ), 0, abort_flag, p.err, lim);
     bool issued = false;
     tc_fence_after();
     const uint64_t qhi = sdesc_sw128(sbase + kSmemQHi, 16, 1024);
     const uint64_t qlo = sdesc_sw128(sbase + kSmemQLo, 16, 1024);
     const uint32_t tO = tmem + kColO;
-    uint32_t li = 0;  // slot loads consumed
-    auto item_ready = [&](uint32_t* s_hi, uint32_t* s_lo) -> bool {
-      *s_hi = li % kSlots;
-      *s_lo = (li + 1) % kSlots;
-      if (!mbar_wait_warp(bar(kBarFull + *s_hi), (li / kSlots) & 1u, abort_flag, p.err, lim))
-        return false;
-      if (!mbar_wait_warp(bar(kBarFull + *s_lo), ((li + 1) / kSlots) & 1u, abort_flag, p.err,
-                          lim))
+    uint32_t ui = 0;  // items consumed
+    auto item_ready = [&](uint32_t* e) -> bool {
+      *e = ui % kItems;
+      if (!mbar_wait_cl_warp(bar(kBarFull + (int)*e), (ui / kItems) & 1u, abort_flag, p.err, lim))
         return false;
       tc_fence_after();
-      li += 2;
+      ++ui;
       return true;
     };
     auto pv = [&](int j) -> bool {  // O (+)= P(j) V(j): hi*hi + hi*lo + lo*hi
-      uint32_t sh, sl;
-      if (!item_ready(&sh, &sl)) return false;
-      if (!mbar_wait_warp(bar(kBarP + (j & 1)), (uint32_t)(j >> 1) & 1u, abort_flag, p.err, lim))
+      uint32_t e;
+      if (!item_ready(&e)) return false;
+      if (!mbar_wait_cl_warp(bar(kBarP + (j & 1)), (uint32_t)(j >> 1) & 1u, abort_flag, p.err, lim))
         return false;
       tc_fence_after();
       const uint32_t tP = tmem + (uint32_t)((j & 1) * kBN);
-      const uint64_t vh = sdesc_sw128(sbase + kSmemRing + sh * kTileBytes, kHalfBytes, 1024);
-      const uint64_t vl = sdesc_sw128(sbase + kSmemRing + sl * kTileBytes, kHalfBytes, 1024);
-      mma8_ts<2048 / 16>(tO, tP, vh, kIdescPV, j > 0 ? 1u : 0u);
-      mma8_ts<2048 / 16>(tO, tP, vl, kIdescPV, 1u);
-      mma8_ts<2048 / 16>(tO, tmem + kColPLo + (uint32_t)((j & 1) * 64), vh, kIdescPV, 1u);
-      tc_commit_elect(bar(kBarEmpty + sh));
-      tc_commit_elect(bar(kBarEmpty + sl));
-      tc_commit_elect(bar(kBarO));
+      const uint32_t ib = sbase + kSmemRing + e * kItemBytes;
+      // this CTA's 64 columns of V: one 128-byte span, 16 keys per step (2048 B)
+      const uint64_t vh = sdesc_sw128(ib, kKSpan, 1024);
+      const uint64_t vl = sdesc_sw128(ib + kPartBytes, kKSpan, 1024);
+      mma8_ts_pair<2048 / 16>(tO, tP, vh, kIdescPV, j > 0 ? 1u : 0u);
+      mma8_ts_pair<2048 / 16>(tO, tP, vl, kIdescPV, 1u);
+      mma8_ts_pair<2048 / 16>(tO, tmem + kColPLo + (uint32_t)((j & 1) * 64), vh, kIdescPV, 1u);
+      tc_commit_pair(bar(kBarEmpty + (int)e));
+      tc_commit_pair(bar(kBarO));
       return true;
     };
     for (int i = 0; i < n && ok; ++i) {
       // S(i) = Q_hi K_hi + Q_hi K_lo + Q_lo K_hi
-      uint32_t sh, sl;
-      if (!(ok = item_ready(&sh, &sl))) break;
+      uint32_t e;
+      if (!(ok = item_ready(&e))) break;
       const uint32_t tS = tmem + (uint32_t)((i & 1) * kBN);
-      const uint64_t kh_d = sdesc_sw128(sbase + kSmemRing + sh * kTileBytes, 16, 1024);
-      const uint64_t kl_d = sdesc_sw128(sbase + kSmemRing + sl * kTileBytes, 16, 1024);
-      mma8_ss_kmajor<kHalfBytes / 16>(tS, qhi, kh_d, kIdescQK, 0u);
-      mma8_ss_kmajor<kHalfBytes / 16>(tS, qhi, kl_d, kIdescQK, 1u);
-      mma8_ss_kmajor<kHalfBytes / 16>(tS, qlo, kh_d, kIdescQK, 1u);
+      const uint32_t ib = sbase + kSmemRing + e * kItemBytes;
+      const uint64_t kh_d = sdesc_sw128(ib, 16, 1024);
+      const uint64_t kl_d = sdesc_sw128(ib + kPartBytes, 16, 1024);
+      mma8_ss_pair<kHalfBytes / 16, kKSpan / 16>(tS, qhi, kh_d, kIdescQK, 0u);
+      mma8_ss_pair<kHalfBytes / 16, kKSpan / 16>(tS, qhi, kl_d, kIdescQK, 1u);
+      mma8_ss_pair<kHalfBytes / 16, kKSpan / 16>(tS, qlo, kh_d, kIdescQK, 1u);
       issued = true;
-      tc_commit_elect(bar(kBarS + (i & 1)));
-      tc_commit_elect(bar(kBarEmpty + sh));
-      tc_commit_elect(bar(kBarEmpty + sl));
+      tc_commit_pair(bar(kBarS + (i & 1)));
+      tc_commit_pair(bar(kBarEmpty + (int)e));
       if (i > 0 && !(ok = pv(i - 1))) break;
     }
     if (ok) ok = pv(n - 1);
     if (issued) {
-      // everything issued must complete before TMEM is freed
-      tc_commit_elect(bar(kBarDrain));
+      // everything issued must complete before either CTA frees its TMEM
+      tc_commit_pair(bar(kBarDrain));
       mbar_wait_warp(bar(kBarDrain), 0, abort_flag, p.err, lim, true);
     }
-  } else if (warp >= 4) {
+  } else if (warp >= 4 && warp < 8) {
     // ------------------------------------------------------------ converters
-    // Warp cw converts rows (keys) 32 cw .. 32 cw + 31 of every tile; lane l
-    // holds elements 4 l .. 4 l + 3 of a row, so each load is one 512-byte row.
+    // K item: this CTA's keys 64 rank .. +63 of the tile; warp cw converts 16
+    // of them, lane l holding elements 4 l .. 4 l + 3 of a row (one 512-byte
+    // row per load).  V item: columns 64 rank .. +63 of all 128 keys; warp cw
+    // converts keys 32 cw .. 32 cw + 31, two rows per load (lanes 0-15 and
+    // 16-31, lane l holding columns 64 rank + 4 (l % 16) .. + 3).
     const int cw = warp - 4;
     const float* kbase = p.k + (int64_t)kh * p.kv_head_stride;
     const float* vbase = p.v + (int64_t)kh * p.kv_head_stride;
     auto row_of = [&](int64_t j) -> int64_t { return p.ring_rows > 0 ? j % p.ring_rows : j; };
     bool ok = true;
-    uint32_t li = 0;  // slot loads written
+    uint32_t ui = 0;  // items written
     // Item u of the ring order -> (V?, key tile).
     auto item_of = [&](int u, int* tile) -> bool {
       if (u == 0) { *tile = 0; return false; }
@@ -283,74 +308,103 @@ __global__ void __launch_bounds__(kThreads, 1) f32x3_d128_kernel(const Params p)
       *tile = (u >> 1) - 1;          // u = 2i: V(i - 1)
       return true;
     };
-    // This warp's 32 rows of item u, as one range of the cache when they are
-    // consecutive and written (else nothing: the loads find them in memory).
-    auto rows_of = [&](int u, const float** ptr) -> bool {
+    // First key and row count of this warp's part of item u.
+    auto part_of = [&](int u, bool* is_v) -> int64_t {
       int tile;
-      const bool is_v = item_of(u, &tile);
-      const int64_t key0 = (kt_first + tile) * kBN + cw * 32;
-      const int64_t row0 = row_of(key0);
-      *ptr = (is_v ? vbase : kbase) + row0 * kD;
-      return key0 + 32 <= L && (p.ring_rows == 0 || row0 + 32 <= p.ring_rows);
+      *is_v = item_of(u, &tile);
+      const int64_t key0 = (kt_first + tile) * kBN;
+      return *is_v ? key0 + 32 * cw : key0 + 64 * rank + 16 * cw;
+    };
+    // Asks L2 for the rows of this warp's part of item u (whole rows; only
+    // when they are written and consecutive in the cache).
+    auto prefetch_part = [&](int u) {
+      bool is_v;
+      const int64_t k0 = part_of(u, &is_v);
+      const int rows = is_v ? 32 : 16;
+      const int64_t r0 = row_of(k0);
+      if (k0 + rows <= L && (p.ring_rows == 0 || r0 + rows <= p.ring_rows))
+        prefetch_l2((is_v ? vbase : kbase) + r0 * kD, (uint32_t)rows * kD * 4u);
     };
     auto item = [&](int u) -> bool {
-      int tile;
-      const float* base = item_of(u, &tile) ? vbase : kbase;
       // Items run ahead of the MMA by about two; ask L2 for the rows of the
       // item after the next now, so that its loads do not wait for DRAM.
-      if (u + 2 < 2 * n && lane == 0) {
-        const float* pf;
-        if (rows_of(u + 2, &pf)) prefetch_l2(pf, 32u * kD * 4u);
-      }
-      const int64_t key0 = (kt_first + tile) * kBN + cw * 32;
-      // Global loads first: their latency overlaps the wait for the slots.
-      // Rows past the written keys read as zeros.  The common case (all 32
-      // rows written, consecutive in the cache) uses one base pointer.
-      float4 x[32];
-      const int64_t row0 = row_of(key0);
-      if (key0 + 32 <= L && (p.ring_rows == 0 || row0 + 32 <= p.ring_rows)) {
-        const float4* src = reinterpret_cast<const float4*>(base + row0 * kD) + lane;
+      if (u + 2 < 2 * n && lane == 0) prefetch_part(u + 2);
+      bool is_v;
+      const int64_t k0 = part_of(u, &is_v);
+      // Global loads first: their latency overlaps the wait for the entry.
+      // Rows past the written keys read as zeros.
+      float4 x[16];
+      if (!is_v) {
+        const float* src = kbase + lane * 4;
+        const int64_t r0 = row_of(k0);
+        if (k0 + 16 <= L && (p.ring_rows == 0 || r0 + 16 <= p.ring_rows)) {
 #pragma unroll
-        for (int r = 0; r < 32; ++r) x[r] = __ldg(src + r * (kD / 4));
+          for (int r = 0; r < 16; ++r) x[r] = __ldg(reinterpret_cast<const float4*>(src + (r0 + r) * kD));
+        } else {
+#pragma unroll
+          for (int r = 0; r < 16; ++r) {
+            x[r] = make_float4(0.f, 0.f, 0.f, 0.f);
+            if (k0 + r < L) x[r] = __ldg(reinterpret_cast<const float4*>(src + row_of(k0 + r) * kD));
+          }
+        }
       } else {
+        const float* src = vbase + 64 * rank + 4 * (lane & 15);
+        const int64_t r0 = row_of(k0);
+        const int sub = lane >> 4;  // row 2 r + sub
+        if (k0 + 32 <= L && (p.ring_rows == 0 || r0 + 32 <= p.ring_rows)) {
 #pragma unroll
-        for (int r = 0; r < 32; ++r) {
-          const int64_t j = key0 + r;
-          x[r] = make_float4(0.f, 0.f, 0.f, 0.f);
-          if (j < L) x[r] = __ldg(reinterpret_cast<const float4*>(base + row_of(j) * kD) + lane);
+          for (int r = 0; r < 16; ++r)
+            x[r] = __ldg(reinterpret_cast<const float4*>(src + (r0 + 2 * r + sub) * kD));
+        } else {
+#pragma unroll
+          for (int r = 0; r < 16; ++r) {
+            const int64_t j = k0 + 2 * r + sub;
+            x[r] = make_float4(0.f, 0.f, 0.f, 0.f);
+            if (j < L) x[r] = __ldg(reinterpret_cast<const float4*>(src + row_of(j) * kD));
+          }
         }
       }
-      const uint32_t s_hi = li % kSlots, s_lo = (li + 1) % kSlots;
-      bool good = mbar_wait(bar(kBarEmpty + s_hi), ((li / kSlots) & 1u) ^ 1u, abort_flag, p.err, lim);
-      good = good && mbar_wait(bar(kBarEmpty + s_lo), (((li + 1) / kSlots) & 1u) ^ 1u, abort_flag,
-                               p.err, lim);
+      const uint32_t e = ui % kItems;
+      const bool good = mbar_wait(bar(kBarEmpty + (int)e), ((ui / kItems) & 1u) ^ 1u, abort_flag,
+                                  p.err, lim);
       if (!__all_sync(0xffffffffu, good)) return false;
-      uint8_t* hi = smem + kSmemRing + s_hi * kTileBytes;
-      uint8_t* lo = smem + kSmemRing + s_lo * kTileBytes;
+      uint8_t* hi = smem + kSmemRing + e * kItemBytes;
+      uint8_t* lo = hi + kPartBytes;
+      if (!is_v) {
 #pragma unroll
-      for (int r = 0; r < 32; ++r) {
-        uint2 h, l;
-        split4(x[r], &h, &l);
-        const uint32_t off = swz_off(cw * 32 + r, lane);
-        *reinterpret_cast<uint2*>(hi + off) = h;
-        *reinterpret_cast<uint2*>(lo + off) = l;
+        for (int r = 0; r < 16; ++r) {
+          uint2 h, l;
+          split4(x[r], &h, &l);
+          const uint32_t off = swz_off<64>(16 * cw + r, lane);
+          *reinterpret_cast<uint2*>(hi + off) = h;
+          *reinterpret_cast<uint2*>(lo + off) = l;
+        }
+      } else {
+        // MN-major: key j at j * 128, 16-byte chunk c (columns 8c .. 8c+7 of
+        // this CTA's 64) at c ^ (j % 8)
+        const int c = (lane & 15) >> 1, half = lane & 1;
+#pragma unroll
+        for (int r = 0; r < 16; ++r) {
+          const int j = 32 * cw + 2 * r + (lane >> 4);
+          uint2 h, l;
+          split4(x[r], &h, &l);
+          const uint32_t off = (uint32_t)(j * 128 + ((c ^ (j & 7)) << 4) + half * 8);
+          *reinterpret_cast<uint2*>(hi + off) = h;
+          *reinterpret_cast<uint2*>(lo + off) = l;
+        }
       }
       fence_proxy_async_smem();
       __syncwarp();
-      if (lane == 0) {
-        mbar_arrive(bar(kBarFull + s_hi));
-        mbar_arrive(bar(kBarFull + s_lo));
-      }
-      li += 2;
+      if (lane == 0) mbar_arrive_cluster(bar_r0(kBarFull + (int)e));
+      ++ui;
       return true;
     };
     if (lane == 0) {
-      const float* pf;
-      if (rows_of(0, &pf)) prefetch_l2(pf, 32u * kD * 4u);
-      if (2 * n > 1 && rows_of(1, &pf)) prefetch_l2(pf, 32u * kD * 4u);
+      prefetch_part(0);
+      if (2 * n > 1) prefetch_part(1);
     }
     for (int u = 0; u < 2 * n && ok; ++u) ok = item(u);
-  } else {
+  } else if (warp < 4) {
     // ------------------------------------------------------------ rows
     const int row = threadIdx.x;  // = TMEM lane
     const int tok = row / p.group;
@@ -372,13 +426,13 @@ __global__ void __launch_bounds__(kThreads, 1) f32x3_d128_kernel(const Params p)
         if (row_valid) x = __ldg(qrow + q4);
         uint2 hv, lv;
         split4(x, &hv, &lv);
-        const uint32_t off = swz_off(row, q4);
+        const uint32_t off = swz_off<128>(row, q4);
         *reinterpret_cast<uint2*>(smem + kSmemQHi + off) = hv;
         *reinterpret_cast<uint2*>(smem + kSmemQLo + off) = lv;
       }
       fence_proxy_async_smem();
       __syncwarp();
-      if (lane == 0) mbar_arrive(bar(kBarQ));
+      if (lane == 0) mbar_arrive_cluster(bar_r0(kBarQ));
     }
 
     bool ok = true;
@@ -498,7 +552,7 @@ __global__ void __launch_bounds__(kThreads, 1) f32x3_d128_kernel(const Params p)
       tmem_wait_st();
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(bar(kBarP + (i & 1)));
+      if (lane == 0) mbar_arrive_cluster(bar_r0(kBarP + (i & 1)));
     }
     if (ok) {
       ok = mbar_wait(bar(kBarO), (uint32_t)(n - 1) & 1u, abort_flag, p.err, lim);
@@ -524,11 +578,14 @@ __global__ void __launch_bounds__(kThreads, 1) f32x3_d128_kernel(const Params p)
     }
   }
 
+  // Neither CTA leaves, nor frees tensor memory, while the pair's products
+  // may still touch it: rank 0 drains them before this point.
   tc_fence_before();
   __syncthreads();
+  cluster_sync();
   if (warp == 8) {
     tc_fence_after();
-    tmem_dealloc(tmem, 512);
+    tmem_dealloc_pair(tmem, 512);
   }
 }
 
@@ -544,8 +601,9 @@ int launch_f32x3_d128(const Call& c) {
   const int group = c.H / c.Hkv;
   const int tok_per_tile = kBM / group;
   const int64_t tiles = (c.T + tok_per_tile - 1) / tok_per_tile;
+  const int64_t pairs = (tiles + 1) / 2;
   const int64_t L = c.start_pos + c.T;
-  if (tiles * c.Hkv > 0x7fffffff || L + kBN > 0x7fffffff) return kErrShape;
+  if (2 * pairs * c.Hkv > 0x7fffffff || L + 2 * kBN > 0x7fffffff) return kErrShape;
   Params p;
   p.q = static_cast<const float*>(c.q);
   p.k = static_cast<const float*>(c.k);
@@ -568,8 +626,23 @@ int launch_f32x3_d128(const Call& c) {
   p.err = c.err;
   p.wait_limit_ns = c.wait_limit_ns;
   p.flags = c.flags;
-  f32x3_d128_kernel<<<dim3((unsigned)(tiles * c.Hkv)), kThreads, kSmemAlloc, c.stream>>>(p);
-  return cudaGetLastError() == cudaSuccess ? kOk : kErrLaunch;
+  // Clusters of two consecutive CTAs: the two query tiles of a pair.
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)(2 * pairs * c.Hkv));
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = kSmemAlloc;
+  cfg.stream = c.stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  if (cudaLaunchKernelEx(&cfg, f32x3_d128_kernel, p) != cudaSuccess ||
+      cudaGetLastError() != cudaSuccess)
+    return kErrLaunch;
+  return kOk;
 }
 
 }  // namespace pfa
