@@ -88,6 +88,7 @@ RING = [
     (100, 50, 8, 2, 128, 64, "bf16", 0, 256, True),         # L <= capacity: not wrapped
     (128, 9000, 8, 2, 512, 1024, "bf16", 512, 1152, True),  # head_dim 512, wrapped
     (60, 700, 8, 2, 64, 40, "f32", 4, 99, True),            # fp32: any capacity >= w + T - 1
+    (60, 700, 8, 2, 128, 40, "f32", 4, 99, True),           # fp32 head_dim 128 (paired CTAs)
     (1, 12345, 8, 2, 128, 128, "bf16", 0, 128, True),       # one token, ring of one tile
 ]
 

@@ -89,9 +89,11 @@ def test_graph_replay_relaxed_capture():
     _prefill(128, False, "relaxed")
 
 
+@pytest.mark.parametrize("D", [64, 128])
 @pytest.mark.parametrize("ring", [False, True])
-def test_graph_entry_fp32_without_capture(ring):
-    _prefill(64, ring, None, dtype="f32")
+def test_graph_entry_fp32_without_capture(D, ring):
+    # head_dim 64: the CUDA-core kernel; 128: the paired tensor-core kernel
+    _prefill(D, ring, None, dtype="f32")
 
 
 def test_graph_lengths_are_checked_on_the_device():
