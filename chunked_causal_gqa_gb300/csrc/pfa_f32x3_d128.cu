@@ -514,13 +514,15 @@ __global__ void __launch_bounds__(kThreads, 1) f32x3_d128_kernel(const Params p)
         uint32_t ph[16], pl[16];
 #pragma unroll
         for (int j = 0; j < 16; ++j) {
-          float xa = __uint_as_float(r[2 * j]) * c, xb = __uint_as_float(r[2 * j + 1]) * c;
+          // s c - base in one fused multiply-add
+          float xa = fmaf(__uint_as_float(r[2 * j]), c, -base);
+          float xb = fmaf(__uint_as_float(r[2 * j + 1]), c, -base);
           if (partial) {
             const int ja = 32 * q + 2 * j;
             if (ja > hi_rel || ja <= lo_rel) xa = -INFINITY;
             if (ja + 1 > hi_rel || ja + 1 <= lo_rel) xb = -INFINITY;
           }
-          const float pa = ex2(xa - base), pb = ex2(xb - base);
+          const float pa = ex2(xa), pb = ex2(xb);
           const uint32_t w = pack_bf16x2(pa, pb);
           ph[j] = w;
           pl[j] = pack_bf16x2(pa - bf16_lo_f32(w), pb - bf16_hi_f32(w));
