@@ -158,6 +158,9 @@ __device__ __forceinline__ uint32_t swz_off(int r, int q) {
   return (uint32_t)(span * (kRows * 128) + r * 128 + ((c ^ (r & 7)) << 4) + half * 8);
 }
 
+// kPosScale (scale > 0): the row maximum is taken over the unscaled scores and
+// scaled once, which leaves the order of the scores unchanged.
+template <bool kPosScale>
 __global__ void __launch_bounds__(kThreads, 1) f32x3_d128_kernel(const Params p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
@@ -468,12 +471,13 @@ __global__ void __launch_bounds__(kThreads, 1) f32x3_d128_kernel(const Params p)
         tmem_wait_ld(r1);
         tmem_wait_ld(r2);
         tmem_wait_ld(r3);
+        const float cs = kPosScale ? 1.f : c;
 #pragma unroll
         for (int j = 0; j < 32; ++j) {
-          x[j] = __uint_as_float(r0[j]) * c;
-          x[32 + j] = __uint_as_float(r1[j]) * c;
-          x[64 + j] = __uint_as_float(r2[j]) * c;
-          x[96 + j] = __uint_as_float(r3[j]) * c;
+          x[j] = __uint_as_float(r0[j]) * cs;
+          x[32 + j] = __uint_as_float(r1[j]) * cs;
+          x[64 + j] = __uint_as_float(r2[j]) * cs;
+          x[96 + j] = __uint_as_float(r3[j]) * cs;
         }
         if (partial) {
 #pragma unroll
@@ -491,6 +495,7 @@ __global__ void __launch_bounds__(kThreads, 1) f32x3_d128_kernel(const Params p)
 #pragma unroll
         for (int q = 0; q < 8; ++q) m[q] = fmaxf(m[q], x[120 + q]);
         mx = max3f(max3f(m[0], m[1], m[2]), max3f(m[3], m[4], m[5]), fmaxf(m[6], m[7]));
+        if (kPosScale) mx *= c;
       }
       // Raise the exponent base only when the new maximum exceeds it by > 2^8.
       float alpha = 1.f;
@@ -596,7 +601,10 @@ __global__ void __launch_bounds__(kThreads, 1) f32x3_d128_kernel(const Params p)
 int launch_f32x3_d128(const Call& c) {
   static DeviceOnce setup;
   const int sr = setup.run(c.device, [] {
-    return cudaFuncSetAttribute(f32x3_d128_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    if (cudaFuncSetAttribute(f32x3_d128_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             kSmemAlloc) != cudaSuccess)
+      return kErrLaunch;
+    return cudaFuncSetAttribute(f32x3_d128_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                 kSmemAlloc) == cudaSuccess ? kOk : kErrLaunch;
   });
   if (sr != kOk) return sr;
@@ -641,7 +649,9 @@ int launch_f32x3_d128(const Call& c) {
   attr[0].val.clusterDim.z = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  if (cudaLaunchKernelEx(&cfg, f32x3_d128_kernel, p) != cudaSuccess ||
+  const cudaError_t e = p.scale_log2 > 0.f ? cudaLaunchKernelEx(&cfg, f32x3_d128_kernel<true>, p)
+                                             : cudaLaunchKernelEx(&cfg, f32x3_d128_kernel<false>, p);
+  if (e != cudaSuccess ||
       cudaGetLastError() != cudaSuccess)
     return kErrLaunch;
   return kOk;
