@@ -123,6 +123,32 @@ struct Params {
 __device__ __forceinline__ float bf16_lo_f32(uint32_t w) { return __uint_as_float(w << 16); }
 __device__ __forceinline__ float bf16_hi_f32(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
 
+// Pairs of fp32 values in one 64-bit register, and the packed pair
+// arithmetic of sm_100+ (each lane rounded as its scalar counterpart).
+__device__ __forceinline__ uint64_t f2_pack(float a, float b) {
+  uint64_t r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(a), "f"(b));
+  return r;
+}
+__device__ __forceinline__ void f2_unpack(uint64_t v, float& a, float& b) {
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(a), "=f"(b) : "l"(v));
+}
+__device__ __forceinline__ uint64_t f2_fma(uint64_t a, uint64_t b, uint64_t c) {
+  uint64_t r;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(r) : "l"(a), "l"(b), "l"(c));
+  return r;
+}
+__device__ __forceinline__ uint64_t f2_sub(uint64_t a, uint64_t b) {
+  uint64_t r;
+  asm("sub.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+  return r;
+}
+__device__ __forceinline__ uint64_t f2_add(uint64_t a, uint64_t b) {
+  uint64_t r;
+  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+  return r;
+}
+
 // Four consecutive fp32 values -> (hi, lo) as two packed bf16 pairs each.
 __device__ __forceinline__ void split4(const float4 x, uint2* hi, uint2* lo) {
   const uint32_t h01 = pack_bf16x2(x.x, x.y), h23 = pack_bf16x2(x.z, x.w);
@@ -510,7 +536,11 @@ __global__ void __launch_bounds__(kThreads, 1) f32x3_d128_kernel(const Params p)
       // P_hi over the first 64 columns of this tile's scores (chunk q lands
       // in columns of chunk q / 2, already read), P_lo in its own columns;
       // l gains the row sum of the fp32 values (4 independent partial sums)
-      float ls[4] = {0.f, 0.f, 0.f, 0.f};
+      // Arithmetic on packed pairs of keys (2j, 2j+1): s c - base, the
+      // residual p - hi, and the row sums (lanes of ls2[0]: even pairs' keys
+      // 2j and 2j+1, of ls2[1]: odd pairs')
+      const uint64_t c2 = f2_pack(c, c), nb2 = f2_pack(-base, -base);
+      uint64_t ls2[2] = {f2_pack(0.f, 0.f), f2_pack(0.f, 0.f)};
 #pragma unroll 1
       for (int q = 0; q < 4; ++q) {
         uint32_t r[32];
@@ -519,9 +549,9 @@ __global__ void __launch_bounds__(kThreads, 1) f32x3_d128_kernel(const Params p)
         uint32_t ph[16], pl[16];
 #pragma unroll
         for (int j = 0; j < 16; ++j) {
-          // s c - base in one fused multiply-add
-          float xa = fmaf(__uint_as_float(r[2 * j]), c, -base);
-          float xb = fmaf(__uint_as_float(r[2 * j + 1]), c, -base);
+          float xa, xb;
+          f2_unpack(f2_fma(f2_pack(__uint_as_float(r[2 * j]), __uint_as_float(r[2 * j + 1])), c2, nb2),
+                    xa, xb);
           if (partial) {
             const int ja = 32 * q + 2 * j;
             if (ja > hi_rel || ja <= lo_rel) xa = -INFINITY;
@@ -530,13 +560,18 @@ __global__ void __launch_bounds__(kThreads, 1) f32x3_d128_kernel(const Params p)
           const float pa = ex2(xa), pb = ex2(xb);
           const uint32_t w = pack_bf16x2(pa, pb);
           ph[j] = w;
-          pl[j] = pack_bf16x2(pa - bf16_lo_f32(w), pb - bf16_hi_f32(w));
-          ls[(2 * j) & 3] += pa;
-          ls[(2 * j + 1) & 3] += pb;
+          const uint64_t pab = f2_pack(pa, pb);
+          float da, db;
+          f2_unpack(f2_sub(pab, f2_pack(bf16_lo_f32(w), bf16_hi_f32(w))), da, db);
+          pl[j] = pack_bf16x2(da, db);
+          ls2[j & 1] = f2_add(ls2[j & 1], pab);
         }
         tmem_st16(tS + 16 * q, ph);
         tmem_st16(tPlo + 16 * q, pl);
       }
+      float ls[4];
+      f2_unpack(ls2[0], ls[0], ls[1]);
+      f2_unpack(ls2[1], ls[2], ls[3]);
       l = l * alpha + ((ls[0] + ls[1]) + (ls[2] + ls[3]));
       if (i > 0) {
         // O is stable once O += P(i-1) V(i-1) has completed.
